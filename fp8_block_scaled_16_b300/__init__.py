@@ -1,0 +1,28 @@
+"""FP8 fine-grained block-quantized linear layer for NVIDIA B300 (sm_103a).
+
+The compute lives in the CUDA library ``libfp8bs.so`` (C ABI:
+``include/fp8bs.h``); ``binding`` marshals torch tensors to it, ``linear``
+chains the calls into one linear layer's forward and backward step, and
+``inputs`` draws the seeded synthetic workloads.  Importing the package does
+not load the library; the first call does, and fails if it is missing.
+"""
+from __future__ import annotations
+
+import importlib
+
+_BINDING_NAMES = (
+    "ROWWISE", "COLWISE_T", "Fp8bsError",
+    "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm_fprop", "fp8bs_gemm_dgrad",
+    "fp8bs_gemm_wgrad", "fp8bs_get_device_status", "fp8bs_status_string", "fp8bs_launch_count",
+    "fp8bs_debug_set_wait_timeout_ns", "fp8bs_debug_set_fault", "fp8bs_debug_e4m3_encode_bits",
+)
+
+__all__ = list(_BINDING_NAMES) + ["Fp8LinearStep"]
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        return getattr(importlib.import_module(".binding", __name__), name)
+    if name == "Fp8LinearStep":
+        return importlib.import_module(".linear", __name__).Fp8LinearStep
+    raise AttributeError(name)

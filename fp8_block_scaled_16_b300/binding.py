@@ -1,0 +1,213 @@
+"""Python binding of the C ABI in include/fp8bs.h (ctypes, argument
+marshalling only).
+
+Each function has the name of the C entry point it calls.  It takes torch
+CUDA tensors, allocates any output the caller did not pass (torch is the
+device-memory allocator here), passes raw device pointers and the current
+CUDA stream to the library, and raises Fp8bsError on a non-OK status.  All
+arithmetic runs in the library's kernels; there is no fallback path: if the
+library is missing or the device is not an sm_103 GPU, the call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+ROWWISE = 1
+COLWISE_T = 2
+
+STATUS = {
+    0: "FP8BS_OK", 1: "FP8BS_ERR_INVALID_ARG", 2: "FP8BS_ERR_SHAPE", 3: "FP8BS_ERR_ALIGN",
+    4: "FP8BS_ERR_ARCH", 5: "FP8BS_ERR_LAUNCH", 6: "FP8BS_ERR_TIMEOUT", 7: "FP8BS_ERR_CUDA",
+}
+
+# Every symbol include/fp8bs.h declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+SIGNATURES = {
+    "fp8bs_quantize_act": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_uint, _P, _P, _P, _P, _P]),
+    "fp8bs_quantize_weight": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "fp8bs_gemm_fprop": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8bs_gemm_dgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8bs_gemm_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8bs_get_device_status": (ctypes.c_int, [_P]),
+    "fp8bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fp8bs_launch_count": (_I64, []),
+    "fp8bs_debug_set_wait_timeout_ns": (ctypes.c_int, [_I64]),
+    "fp8bs_debug_set_fault": (ctypes.c_int, [ctypes.c_int]),
+    "fp8bs_debug_e4m3_encode_bits": (ctypes.c_int, [ctypes.c_uint32, _I64, _P, _P]),
+}
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libfp8bs.so (built in-tree by build.py).  Raises if it is
+    missing: there is no other implementation to fall back to."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -m fp8_block_scaled_16_b300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise Fp8bsError(rc, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, shape, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _out(t: Optional[torch.Tensor], shape, dtype, device) -> torch.Tensor:
+    return torch.empty(shape, dtype=dtype, device=device) if t is None else t
+
+
+# ---------------------------------------------------------------- entry points
+
+def fp8bs_quantize_act(x: torch.Tensor, flags: int = ROWWISE, q=None, s=None, qT=None, sT=None,
+                       stream=None) -> Tuple[Optional[torch.Tensor], ...]:
+    """x BF16 [rows][cols] -> (q u8 [rows][cols], s f32 [cols/128][rows],
+    qT u8 [cols][rows], sT f32 [rows/128][cols]); the pair for a layout that
+    `flags` does not request is (None, None)."""
+    rows, cols = x.shape
+    dev = x.device
+    xp = _dev(x, torch.bfloat16, (rows, cols), "x")
+    ptrs = [None, None, None, None]
+    if flags & ROWWISE:
+        q = _out(q, (rows, cols), torch.uint8, dev)
+        s = _out(s, (cols // 128, rows), torch.float32, dev)
+        ptrs[0] = _dev(q, torch.uint8, (rows, cols), "q")
+        ptrs[1] = _dev(s, torch.float32, (cols // 128, rows), "s")
+    else:
+        q = s = None
+    if flags & COLWISE_T:
+        qT = _out(qT, (cols, rows), torch.uint8, dev)
+        sT = _out(sT, (rows // 128, cols), torch.float32, dev)
+        ptrs[2] = _dev(qT, torch.uint8, (cols, rows), "qT")
+        ptrs[3] = _dev(sT, torch.float32, (rows // 128, cols), "sT")
+    else:
+        qT = sT = None
+    _check(load().fp8bs_quantize_act(xp, rows, cols, flags, *ptrs, _stream(stream)), "fp8bs_quantize_act")
+    return q, s, qT, sT
+
+
+def fp8bs_quantize_weight(w: torch.Tensor, q=None, qT=None, s=None, want_t: bool = True, stream=None):
+    """w BF16 [n][k] -> (q u8 [n][k], qT u8 [k][n] or None, s f32 [n/128][k/128])."""
+    n, k = w.shape
+    dev = w.device
+    wp = _dev(w, torch.bfloat16, (n, k), "w")
+    q = _out(q, (n, k), torch.uint8, dev)
+    s = _out(s, (n // 128, k // 128), torch.float32, dev)
+    if want_t:
+        qT = _out(qT, (k, n), torch.uint8, dev)
+    qTp = _dev(qT, torch.uint8, (k, n), "qT") if qT is not None else None
+    _check(load().fp8bs_quantize_weight(wp, n, k, _dev(q, torch.uint8, (n, k), "q"), qTp,
+                                        _dev(s, torch.float32, (n // 128, k // 128), "s"), _stream(stream)),
+           "fp8bs_quantize_weight")
+    return q, qT, s
+
+
+def fp8bs_gemm_fprop(xq, sx, wq, sw, y=None, stream=None) -> torch.Tensor:
+    """Y [M][N] BF16 = X W^T from Xq [M][K], sx [K/128][M], Wq [N][K], sw [N/128][K/128]."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    y = _out(y, (M, N), torch.bfloat16, xq.device)
+    _check(load().fp8bs_gemm_fprop(
+        _dev(xq, torch.uint8, (M, K), "xq"), _dev(sx, torch.float32, (K // 128, M), "sx"),
+        _dev(wq, torch.uint8, (N, K), "wq"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
+        _dev(y, torch.bfloat16, (M, N), "y"), M, N, K, _stream(stream)), "fp8bs_gemm_fprop")
+    return y
+
+
+def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None) -> torch.Tensor:
+    """dX [M][K] BF16 = dY W from dYq [M][N], sdy [N/128][M], WqT [K][N], sw [N/128][K/128]."""
+    M, N = dyq.shape
+    K = wqT.shape[0]
+    dx = _out(dx, (M, K), torch.bfloat16, dyq.device)
+    _check(load().fp8bs_gemm_dgrad(
+        _dev(dyq, torch.uint8, (M, N), "dyq"), _dev(sdy, torch.float32, (N // 128, M), "sdy"),
+        _dev(wqT, torch.uint8, (K, N), "wqT"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
+        _dev(dx, torch.bfloat16, (M, K), "dx"), M, N, K, _stream(stream)), "fp8bs_gemm_dgrad")
+    return dx
+
+
+def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None) -> torch.Tensor:
+    """dW [N][K] BF16 = dY^T X from dYTq [N][M], sdyT [M/128][N], XTq [K][M], sxT [M/128][K]."""
+    N, M = dyTq.shape
+    K = xTq.shape[0]
+    dw = _out(dw, (N, K), torch.bfloat16, dyTq.device)
+    _check(load().fp8bs_gemm_wgrad(
+        _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
+        _dev(xTq, torch.uint8, (K, M), "xTq"), _dev(sxT, torch.float32, (M // 128, K), "sxT"),
+        _dev(dw, torch.bfloat16, (N, K), "dw"), M, N, K, _stream(stream)), "fp8bs_gemm_wgrad")
+    return dw
+
+
+def fp8bs_get_device_status(stream=None) -> int:
+    return int(load().fp8bs_get_device_status(_stream(stream)))
+
+
+def fp8bs_status_string(status: int) -> str:
+    return load().fp8bs_status_string(status).decode()
+
+
+def fp8bs_launch_count() -> int:
+    return int(load().fp8bs_launch_count())
+
+
+def fp8bs_debug_set_wait_timeout_ns(ns: int) -> None:
+    _check(load().fp8bs_debug_set_wait_timeout_ns(ns), "fp8bs_debug_set_wait_timeout_ns")
+
+
+def fp8bs_debug_set_fault(mode: int) -> None:
+    _check(load().fp8bs_debug_set_fault(mode), "fp8bs_debug_set_fault")
+
+
+def fp8bs_debug_e4m3_encode_bits(first: int, n: int, out: Optional[torch.Tensor] = None, stream=None):
+    out = _out(out, (n,), torch.uint8, torch.device("cuda"))
+    _check(load().fp8bs_debug_e4m3_encode_bits(first, n, _dev(out, torch.uint8, (n,), "out"), _stream(stream)),
+           "fp8bs_debug_e4m3_encode_bits")
+    return out

@@ -1,0 +1,309 @@
+// fp8bs.cu -- host side of the C ABI declared in include/fp8bs.h: argument
+// validation, TMA tensor-map encoding, kernel launches on the caller's
+// stream, and the per-device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fp8bs.h"
+#include "gemm.cuh"
+#include "quant.cuh"
+
+namespace fp8bs {
+
+// Per-device status word written by kernels that give up a bounded wait.
+__device__ uint32_t g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+
+std::atomic<int64_t> g_launches{0};
+std::atomic<int64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_fault{0};
+
+struct DeviceInfo {
+    bool ready = false;
+    bool arch_ok = false;
+    int sm_count = 0;
+    uint32_t* status = nullptr;
+    bool gemm_attr_set[2] = {false, false};
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dim_ok(int64_t d) { return d > 0 && (d % 128) == 0 && d <= (int64_t(1) << 31); }
+
+// Looks up (once per device) whether this device can run the sm_103a
+// kernels, its SM count and the device address of the status word.
+int current_device(DeviceInfo** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FP8BS_ERR_ARCH;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_ARCH;
+        }
+        d.arch_ok = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        if (d.arch_ok) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+                cudaGetLastError();
+                return FP8BS_ERR_LAUNCH;
+            }
+            d.status = static_cast<uint32_t*>(p);
+        }
+        d.ready = true;
+    }
+    if (!d.arch_ok) return FP8BS_ERR_ARCH;
+    *out = &d;
+    return FP8BS_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        cudaGetLastError();
+    });
+    return g_encode;
+}
+
+// 2-D row-major tensor [outer][inner] of `elem` bytes per element.
+bool tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto fn = encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+}
+
+// C[rows][cols] = block-scaled A[rows][kc] * B[cols][kc]^T (see gemm.cuh).
+int run_gemm(int sbmode, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
+             const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
+             cudaStream_t st) {
+    using namespace gemm;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+
+    CUtensorMap tmA, tmB, tmSA, tmSB;
+    const uint64_t kblocks = static_cast<uint64_t>(kc / BK);
+    if (!tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kc, rows, kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kc, cols, kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tmap_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sa, rows, kblocks, rows * 4, SA_FLOATS, 1,
+                 CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8BS_ERR_LAUNCH;
+    if (sbmode == SB_VECTOR) {
+        if (!tmap_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sb, cols, kblocks, cols * 4, SB_FLOATS, 1,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+            return FP8BS_ERR_LAUNCH;
+    } else {
+        tmSB = tmSA;
+    }
+
+    Params p;
+    p.m_tiles = static_cast<int32_t>(rows / BM);
+    p.n_tiles = static_cast<int32_t>((cols + BN - 1) / BN);
+    p.kblocks = static_cast<int32_t>(kblocks);
+    p.nb_valid = static_cast<int32_t>(cols / 128);
+    p.cols = cols;
+    p.sb = sb;
+    p.sb_stride_j = sb_stride_j;
+    p.sb_stride_b = sb_stride_b;
+    p.out = static_cast<uint16_t*>(out);
+    p.status = d->status;
+    p.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
+    p.fault = g_fault.exchange(0);
+
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    if (tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
+    const int grid = static_cast<int>(tiles < d->sm_count ? tiles : d->sm_count);
+
+    auto kern = (sbmode == SB_VECTOR) ? gemm_kernel<SB_VECTOR> : gemm_kernel<SB_SCALAR>;
+    if (!d->gemm_attr_set[sbmode]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+            return launch_status();
+        d->gemm_attr_set[sbmode] = true;
+    }
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmSA, tmSB, p);
+    g_launches.fetch_add(1);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" {
+
+int fp8bs_quantize_act(const void* x, int64_t rows, int64_t cols, unsigned flags, uint8_t* q, float* s,
+                       uint8_t* qT, float* sT, void* stream) {
+    const bool row = (flags & FP8BS_ROWWISE) != 0, colt = (flags & FP8BS_COLWISE_T) != 0;
+    if (!x || (flags & ~(FP8BS_ROWWISE | FP8BS_COLWISE_T)) || (!row && !colt)) return FP8BS_ERR_INVALID_ARG;
+    if ((row && (!q || !s)) || (colt && (!qT || !sT))) return FP8BS_ERR_INVALID_ARG;
+    if (!dim_ok(rows) || !dim_ok(cols) || rows / 128 > 65535) return FP8BS_ERR_SHAPE;
+    if (!aligned16(x) || (row && (!aligned16(q) || !aligned16(s))) || (colt && (!aligned16(qT) || !aligned16(sT))))
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    const dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
+    const auto* xw = static_cast<const uint32_t*>(x);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (row && colt)
+        quant_tile_kernel<QM_ROW | QM_COLT><<<grid, 256, 0, st>>>(xw, rows, cols, q, s, qT, sT);
+    else if (row)
+        quant_tile_kernel<QM_ROW><<<grid, 256, 0, st>>>(xw, rows, cols, q, s, nullptr, nullptr);
+    else
+        quant_tile_kernel<QM_COLT><<<grid, 256, 0, st>>>(xw, rows, cols, nullptr, nullptr, qT, sT);
+    g_launches.fetch_add(1);
+    return launch_status();
+}
+
+int fp8bs_quantize_weight(const void* w, int64_t n, int64_t k, uint8_t* q, uint8_t* qT, float* s, void* stream) {
+    if (!w || !q || !s) return FP8BS_ERR_INVALID_ARG;
+    if (!dim_ok(n) || !dim_ok(k) || n / 128 > 65535) return FP8BS_ERR_SHAPE;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(s) || (qT && !aligned16(qT))) return FP8BS_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    const dim3 grid(static_cast<unsigned>(k / 128), static_cast<unsigned>(n / 128));
+    quant_tile_kernel<QM_BLOCK><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint32_t*>(w), n, k, q, s, qT, nullptr);
+    g_launches.fetch_add(1);
+    return launch_status();
+}
+
+static int check_gemm_args(const void* a, const void* sa, const void* b, const void* sb, const void* out,
+                           int64_t M, int64_t N, int64_t K) {
+    if (!a || !sa || !b || !sb || !out) return FP8BS_ERR_INVALID_ARG;
+    if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return FP8BS_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out)) return FP8BS_ERR_ALIGN;
+    return FP8BS_OK;
+}
+
+int fp8bs_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, void* y, int64_t M,
+                     int64_t N, int64_t K, void* stream) {
+    int rc = check_gemm_args(xq, sx, wq, sw, y, M, N, K);
+    if (rc != FP8BS_OK) return rc;
+    // A = Xq [M][K] (row scales sx [K/128][M]); B = Wq [N][K]; the B scale of
+    // output column block jb and K block b is sw[jb][b].
+    return run_gemm(gemm::SB_SCALAR, xq, wq, M, N, K, sx, sw, K / 128, 1, y, static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw, void* dx,
+                     int64_t M, int64_t N, int64_t K, void* stream) {
+    int rc = check_gemm_args(dyq, sdy, wqT, sw, dx, M, N, K);
+    if (rc != FP8BS_OK) return rc;
+    // A = dYq [M][N] (row scales sdy [N/128][M]); B = WqT [K][N]; contraction
+    // block b is a 128-row block of W, output column block jb a 128-column
+    // block of W: scale sw[b][jb].
+    return run_gemm(gemm::SB_SCALAR, dyq, wqT, M, K, N, sdy, sw, 1, K / 128, dx, static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT, void* dw,
+                     int64_t M, int64_t N, int64_t K, void* stream) {
+    int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
+    if (rc != FP8BS_OK) return rc;
+    // A = dYTq [N][M] (row scales sdyT [M/128][N]); B = XTq [K][M] with a
+    // per-column scale vector sxT [M/128][K].
+    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, M, sdyT, sxT, 0, 0, dw, static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_get_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    uint32_t v = 0, zero = 0;
+    if (cudaMemcpy(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    return (v & kStatusTimeout) ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
+}
+
+const char* fp8bs_status_string(int status) {
+    switch (status) {
+        case FP8BS_OK: return "FP8BS_OK";
+        case FP8BS_ERR_INVALID_ARG: return "FP8BS_ERR_INVALID_ARG";
+        case FP8BS_ERR_SHAPE: return "FP8BS_ERR_SHAPE";
+        case FP8BS_ERR_ALIGN: return "FP8BS_ERR_ALIGN";
+        case FP8BS_ERR_ARCH: return "FP8BS_ERR_ARCH";
+        case FP8BS_ERR_LAUNCH: return "FP8BS_ERR_LAUNCH";
+        case FP8BS_ERR_TIMEOUT: return "FP8BS_ERR_TIMEOUT";
+        case FP8BS_ERR_CUDA: return "FP8BS_ERR_CUDA";
+        default: return "FP8BS_ERR_UNKNOWN";
+    }
+}
+
+int64_t fp8bs_launch_count(void) { return g_launches.load(); }
+
+int fp8bs_debug_set_wait_timeout_ns(int64_t ns) {
+    if (ns < 0) return FP8BS_ERR_INVALID_ARG;
+    g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
+    return FP8BS_OK;
+}
+
+int fp8bs_debug_set_fault(int mode) {
+    if (mode != 0 && mode != 1) return FP8BS_ERR_INVALID_ARG;
+    g_fault.store(mode);
+    return FP8BS_OK;
+}
+
+int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* stream) {
+    if (!out || n < 0) return FP8BS_ERR_INVALID_ARG;
+    if (n > (int64_t(1) << 32) || static_cast<uint64_t>(first) + static_cast<uint64_t>(n) > (uint64_t(1) << 32))
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(out)) return FP8BS_ERR_ALIGN;
+    if (n == 0) return FP8BS_OK;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    const int64_t groups = (n + 3) / 4;
+    const int64_t want = (groups + 255) / 256;
+    const int grid = static_cast<int>(want < 8 * d->sm_count ? want : 8 * d->sm_count);
+    e4m3_encode_bits_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(first, n, out);
+    g_launches.fetch_add(1);
+    return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+// quant.cuh -- HBM-bound fused amax + scale + E4M3 cast for the three tile
+// shapes of the fine-grained block quantization (1x128 activation tiles,
+// 128x1 token-dim tiles written transposed, 128x128 weight blocks).
+//
+// One CTA owns one 128x128 BF16 tile of the input (32 KB): it stages the
+// tile in shared memory with 16-byte coalesced loads, then computes
+//   - row maxima (1x128 tiles) with a bank-skewed row sweep,
+//   - column maxima (128x1 tiles, or the 128x128 block) with a column sweep
+//     whose 32 words per thread stay in registers for the transposed cast,
+// on the BF16 bit patterns (|x| ordering equals the ordering of the
+// sign-cleared bits, so a packed 16-bit unsigned max is exact), then one
+// IEEE division pair per tile for s = amax/448 and inv = 448/amax, then
+// the cast q = E4M3_rne_satfinite(x * inv) and packed, coalesced stores.
+// Because every stored value is an exact function of the BF16 input (an
+// exact max, correctly rounded divisions and multiply, a correctly rounded
+// conversion), the output is bit-identical to a scalar implementation of
+// the same formulas.
+#pragma once
+
+#include <cfloat>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8bs {
+
+enum : int { QM_ROW = 1, QM_COLT = 2, QM_BLOCK = 4 };
+
+// s = amax/448 and inv = 448/amax, both IEEE round-to-nearest; an all-zero
+// tile gets s = inv = 1; an overflowing inv is clamped to FLT_MAX.
+__device__ __forceinline__ void tile_scale(float amax, float& s, float& inv) {
+    if (amax == 0.0f) {
+        s = 1.0f;
+        inv = 1.0f;
+        return;
+    }
+    s = __fdiv_rn(amax, 448.0f);
+    inv = fminf(__fdiv_rn(448.0f, amax), FLT_MAX);
+}
+
+__device__ __forceinline__ uint32_t e4m3x4_lo(uint32_t w0, uint32_t w1, float iv) {
+    // low BF16 halves of two words: elements (w0.lo, w1.lo)
+    return e4m3x2(__fmul_rn(bf16lo_to_f32(w0), iv), __fmul_rn(bf16lo_to_f32(w1), iv));
+}
+__device__ __forceinline__ uint32_t e4m3x4_hi(uint32_t w0, uint32_t w1, float iv) {
+    return e4m3x2(__fmul_rn(bf16hi_to_f32(w0), iv), __fmul_rn(bf16hi_to_f32(w1), iv));
+}
+
+// x: BF16 [rows][cols] viewed as 32-bit words (two BF16 per word).
+// MODE & QM_ROW   : q [rows][cols], s [cols/128][rows]
+// MODE & QM_COLT  : qT [cols][rows], sT [rows/128][cols]
+// MODE == QM_BLOCK: q [rows][cols], qT [cols][rows] (nullable),
+//                   s [rows/128][cols/128]
+template <int MODE>
+__global__ void __launch_bounds__(256) quant_tile_kernel(const uint32_t* __restrict__ x, int64_t rows,
+                                                         int64_t cols, uint8_t* __restrict__ q,
+                                                         float* __restrict__ s, uint8_t* __restrict__ qT,
+                                                         float* __restrict__ sT) {
+    constexpr bool kRow = (MODE & QM_ROW) != 0;
+    constexpr bool kColT = (MODE & QM_COLT) != 0;
+    constexpr bool kBlock = (MODE & QM_BLOCK) != 0;
+    constexpr bool kNeedCol = kColT || kBlock;
+
+    __shared__ __align__(16) uint32_t tile[128 * 64];
+    __shared__ uint32_t rmax[128];
+    __shared__ float rinv[128];
+    __shared__ uint32_t cpart[4][64];
+    __shared__ float cinv[128];
+    __shared__ float binv;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+    const int64_t wpr = cols >> 1;  // words per row
+
+    // 1. The 128x128 tile into shared memory: 2048 chunks of 16 bytes, eight
+    //    per thread, all loads issued before the first use.
+    {
+        const uint32_t* src = x + r0 * wpr + (c0 >> 1);
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int id = i * 256 + tid, r = id >> 4, ch = id & 15;
+            v[i] = ld_nc_v4(src + r * wpr + ch * 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int id = i * 256 + tid, r = id >> 4, ch = id & 15;
+            *reinterpret_cast<uint4*>(&tile[r * 64 + ch * 4]) = v[i];
+        }
+    }
+    __syncthreads();
+
+    // 2a. Column sweep: thread -> column pair cp (columns 2cp, 2cp+1), rows
+    //     [32 seg, 32 seg + 32).  Lanes read consecutive words: no conflicts.
+    const int cp = tid & 63, seg = tid >> 6;
+    uint32_t cw[kNeedCol ? 32 : 1];
+    if constexpr (kNeedCol) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+            cw[i] = tile[(seg * 32 + i) * 64 + cp];
+            m = max_u16x2(m, cw[i] & 0x7FFF7FFFu);
+        }
+        cpart[seg][cp] = m;
+    }
+    // 2b. Row sweep: thread -> row tid/2, half tid%2; word order skewed by
+    //     lane so the 32 lanes hit 32 different banks.
+    if constexpr (kRow) {
+        const int r = tid >> 1, h = tid & 1;
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < 32; j++) m = max_u16x2(m, tile[r * 64 + h * 32 + ((j + lane) & 31)] & 0x7FFF7FFFu);
+        m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        if (h == 0) rmax[r] = max(m & 0xFFFFu, m >> 16);
+    }
+    __syncthreads();
+
+    // 3. Scales: one division pair per tile, spread over 128 threads.
+    if constexpr (kRow) {
+        if (tid < 128) {
+            float sc, iv;
+            tile_scale(__uint_as_float(rmax[tid] << 16), sc, iv);
+            rinv[tid] = iv;
+            s[static_cast<int64_t>(blockIdx.x) * rows + r0 + tid] = sc;
+        }
+    }
+    if constexpr (kColT) {
+        if (tid < 128) {
+            const int p = tid >> 1;
+            uint32_t m = max_u16x2(max_u16x2(cpart[0][p], cpart[1][p]), max_u16x2(cpart[2][p], cpart[3][p]));
+            const uint32_t bits = (tid & 1) ? (m >> 16) : (m & 0xFFFFu);
+            float sc, iv;
+            tile_scale(__uint_as_float(bits << 16), sc, iv);
+            cinv[tid] = iv;
+            sT[static_cast<int64_t>(blockIdx.y) * cols + c0 + tid] = sc;
+        }
+    }
+    if constexpr (kBlock) {
+        if (warp == 0) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) m = max_u16x2(m, (&cpart[0][0])[i * 32 + lane]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) {
+                float sc, iv;
+                tile_scale(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16), sc, iv);
+                binv = iv;
+                s[static_cast<int64_t>(blockIdx.y) * (cols >> 7) + blockIdx.x] = sc;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 4a. Row-layout payload (1x128 tiles, or the weight block): warp w
+    //     writes rows [16w, 16w+16), lane l owns elements [4l, 4l+4): one
+    //     128-byte store per row.
+    if constexpr (kRow || kBlock) {
+#pragma unroll 4
+        for (int i = 0; i < 16; i++) {
+            const int r = warp * 16 + i;
+            const uint2 w2 = *reinterpret_cast<const uint2*>(&tile[r * 64 + 2 * lane]);
+            const float iv = kRow ? rinv[r] : binv;
+            const uint32_t lo = e4m3x2(__fmul_rn(bf16lo_to_f32(w2.x), iv), __fmul_rn(bf16hi_to_f32(w2.x), iv));
+            const uint32_t hi = e4m3x2(__fmul_rn(bf16lo_to_f32(w2.y), iv), __fmul_rn(bf16hi_to_f32(w2.y), iv));
+            *reinterpret_cast<uint32_t*>(q + (r0 + r) * cols + c0 + 4 * lane) = lo | (hi << 16);
+        }
+    }
+
+    // 4b. Transposed payload: thread (cp, seg) writes 32 bytes of qT rows
+    //     2cp and 2cp+1 (tokens [32 seg, 32 seg + 32) of this tile).
+    if constexpr (kNeedCol) {
+        if (kColT || qT != nullptr) {
+            const float ivl = kColT ? cinv[2 * cp] : binv;
+            const float ivh = kColT ? cinv[2 * cp + 1] : binv;
+            uint32_t pl[8], ph[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                pl[i] = e4m3x4_lo(cw[4 * i], cw[4 * i + 1], ivl) | (e4m3x4_lo(cw[4 * i + 2], cw[4 * i + 3], ivl) << 16);
+                ph[i] = e4m3x4_hi(cw[4 * i], cw[4 * i + 1], ivh) | (e4m3x4_hi(cw[4 * i + 2], cw[4 * i + 3], ivh) << 16);
+            }
+            uint8_t* dl = qT + (c0 + 2 * cp) * rows + r0 + seg * 32;
+            uint8_t* dh = dl + rows;
+            reinterpret_cast<uint4*>(dl)[0] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            reinterpret_cast<uint4*>(dl)[1] = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+            reinterpret_cast<uint4*>(dh)[0] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+            reinterpret_cast<uint4*>(dh)[1] = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+        }
+    }
+}
+
+// FP32 bit patterns [first, first+n) -> E4M3 codes, through the same
+// conversion the quantizers use (pairs of values per instruction).
+__global__ void e4m3_encode_bits_kernel(uint32_t first, int64_t n, uint8_t* __restrict__ out) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 4;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4; i < n; i += stride) {
+        const uint32_t b = first + static_cast<uint32_t>(i);
+        if (i + 4 <= n) {
+            const uint32_t lo = e4m3x2(__uint_as_float(b), __uint_as_float(b + 1));
+            const uint32_t hi = e4m3x2(__uint_as_float(b + 2), __uint_as_float(b + 3));
+            *reinterpret_cast<uint32_t*>(out + i) = lo | (hi << 16);
+        } else {
+            for (int64_t j = i; j < n; j++)
+                out[j] = static_cast<uint8_t>(e4m3x2(__uint_as_float(first + static_cast<uint32_t>(j)), 0.0f));
+        }
+    }
+}
+
+}  // namespace fp8bs

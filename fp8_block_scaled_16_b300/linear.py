@@ -1,0 +1,73 @@
+"""One FP8 block-scaled linear layer, forward and backward, as a fixed
+sequence of library calls on preallocated device buffers.
+
+    forward : X -> (Xq, sX) [1x128] and (XTq, sXT) [128x1, transposed] in one
+              read of X; W -> (Wq, WqT, sW) [128x128]; Y = X W^T
+    backward: dY -> (dYq, sdY) and (dYTq, sdYT) in one read of dY;
+              dX = dY W; dW = dY^T X
+
+This is the linear-layer GEMM path the Puro-2B pages put on blockwise FP8
+(blog section "FP8：加快 RTX 5090 上的训练"; arXiv part 1/7, section 2.1):
+the main GEMMs of forward and backward, with activations requantized along
+tokens for the weight gradient.  The weight is quantized inside every step
+here; a trainer that keeps W fixed across micro-batches may quantize it once.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class Fp8LinearStep:
+    """Buffers for one linear of shape x [M][K], w [N][K] and the calls of
+    one training step over them."""
+
+    def __init__(self, M: int, N: int, K: int, device="cuda", ops=("fprop", "dgrad", "wgrad")):
+        self.M, self.N, self.K, self.ops = M, N, K, tuple(ops)
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        need_t = "wgrad" in self.ops
+        self.xq, self.sx = e((M, K), u8), e((K // 128, M), f32)
+        self.xTq, self.sxT = (e((K, M), u8), e((M // 128, K), f32)) if need_t else (None, None)
+        self.wq, self.sw = e((N, K), u8), e((N // 128, K // 128), f32)
+        self.wqT = e((K, N), u8) if "dgrad" in self.ops else None
+        self.y = e((M, N), bf)
+        bwd = "dgrad" in self.ops or "wgrad" in self.ops
+        self.dyq, self.sdy = (e((M, N), u8), e((N // 128, M), f32)) if "dgrad" in self.ops else (None, None)
+        self.dyTq, self.sdyT = (e((N, M), u8), e((M // 128, N), f32)) if need_t else (None, None)
+        self.dx = e((M, K), bf) if "dgrad" in self.ops else None
+        self.dw = e((N, K), bf) if "wgrad" in self.ops else None
+        self.has_bwd = bwd
+
+    def launches_per_step(self) -> int:
+        n = 3  # quantize X, quantize W, fprop
+        if self.has_bwd:
+            n += 1  # quantize dY
+        n += ("dgrad" in self.ops) + ("wgrad" in self.ops)
+        return n
+
+    def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
+        flags = B.ROWWISE | (B.COLWISE_T if "wgrad" in self.ops else 0)
+        B.fp8bs_quantize_act(x, flags, self.xq, self.sx, self.xTq, self.sxT, stream=stream)
+        B.fp8bs_quantize_weight(w, self.wq, self.wqT, self.sw, want_t="dgrad" in self.ops, stream=stream)
+        return B.fp8bs_gemm_fprop(self.xq, self.sx, self.wq, self.sw, self.y, stream=stream)
+
+    def backward(self, dy: Optional[torch.Tensor], stream=None):
+        if not self.has_bwd:
+            return None, None
+        flags = (B.ROWWISE if "dgrad" in self.ops else 0) | (B.COLWISE_T if "wgrad" in self.ops else 0)
+        B.fp8bs_quantize_act(dy, flags, self.dyq, self.sdy, self.dyTq, self.sdyT, stream=stream)
+        dx = dw = None
+        if "dgrad" in self.ops:
+            dx = B.fp8bs_gemm_dgrad(self.dyq, self.sdy, self.wqT, self.sw, self.dx, stream=stream)
+        if "wgrad" in self.ops:
+            dw = B.fp8bs_gemm_wgrad(self.dyTq, self.sdyT, self.xTq, self.sxT, self.dw, stream=stream)
+        return dx, dw
+
+    def step(self, x, w, dy=None, stream=None):
+        y = self.forward(x, w, stream=stream)
+        dx, dw = self.backward(dy, stream=stream)
+        return y, dx, dw

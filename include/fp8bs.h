@@ -1,0 +1,169 @@
+/*
+ * fp8bs.h -- C ABI of the FP8 fine-grained block-quantized linear layer for
+ * NVIDIA B300 (sm_103a).
+ *
+ * The method.  The Puro-2B pages put the main Transformer linear-layer GEMMs
+ * on a blockwise FP8 path that follows DeepSeek-V3's fine-grained block
+ * quantization, and keep numerically sensitive operations and the training
+ * state in BF16/FP32 ("Puro-2B: 普通实验室也能做预训练？", section
+ * "FP8：加快 RTX 5090 上的训练"; "Puro-2B: Poor Lab's Qwen2-1.5B Trained on
+ * RTX 5090 within $5090", part 1/7, section 2.1 and section 1 item 2; bit.fan
+ * news article, section "FP8 training and its trade-off").  The pages print
+ * none of the scheme's parameters; this library implements its published
+ * DeepSeek-V3 form:
+ *   - activations: one FP32 scale per 1x128 tile (a row segment of 128
+ *     elements along the contraction dimension);
+ *   - weights: one FP32 scale per 128x128 block;
+ *   - scale s = amax / 448 (FP32 division); payload q = E4M3(x * (448/amax))
+ *     with one rounded FP32 multiply, round-to-nearest-even, saturating at
+ *     +-448 (OCP E4M3FN); an all-zero tile stores s = 1; when 448/amax
+ *     overflows FP32 the multiplier is clamped to FLT_MAX;
+ *   - GEMMs: each 128-wide K block's partial sum P_b comes from the tensor
+ *     cores in FP32 and is promoted outside them:
+ *     acc = fma(P_b, sa_b * sb_b, acc), then the output is rounded to BF16;
+ *   - weight gradient: X and dY are requantized along the token dimension
+ *     (128x1 tiles) from their BF16 originals and stored transposed, so the
+ *     token dimension becomes the contraction dimension.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are row-major and contiguous; "[a][b]" means a rows of b.
+ *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
+ *     memory) on the current device, 16-byte aligned.  The caller owns every
+ *     buffer; the library never allocates or frees per call.
+ *   - Every dimension must be a positive multiple of 128.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous and stream-ordered; the host never synchronizes.
+ *   - Argument errors return a status and launch nothing.  Errors that
+ *     happen on the device (a bounded wait that expired) are recorded in a
+ *     per-device status word read by fp8bs_get_device_status().
+ *   - Outputs are bitwise deterministic (no atomics, fixed reduction order).
+ *   - Calls on different streams are thread-safe; output buffers of calls
+ *     that may overlap in time must not alias.
+ */
+#ifndef FP8BS_H_
+#define FP8BS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8bs_status {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = 1, /* a required pointer is NULL, or bad flags */
+    FP8BS_ERR_SHAPE = 2,       /* a dimension is <= 0, not a multiple of 128, or too large */
+    FP8BS_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    FP8BS_ERR_ARCH = 4,        /* no CUDA device, or the device is not sm_103 / sm_100 family */
+    FP8BS_ERR_LAUNCH = 5,      /* the CUDA runtime reported an error at launch */
+    FP8BS_ERR_TIMEOUT = 6,     /* a bounded wait inside a kernel expired (device status) */
+    FP8BS_ERR_CUDA = 7         /* a CUDA runtime call failed (device status query) */
+} fp8bs_status;
+
+/* Layout flags for fp8bs_quantize_act (may be OR-ed: one read of x then
+ * writes both layouts). */
+#define FP8BS_ROWWISE 1u   /* 1x128 tiles: q [rows][cols], s [cols/128][rows] */
+#define FP8BS_COLWISE_T 2u /* 128x1 tiles, transposed: qT [cols][rows], sT [rows/128][cols] */
+
+/*
+ * Activation (or activation-gradient) quantization.
+ *   x      : BF16 [rows][cols], read only.
+ *   flags  : FP8BS_ROWWISE and/or FP8BS_COLWISE_T (at least one).
+ *   q, s   : with FP8BS_ROWWISE -- E4M3 payload [rows][cols] and FP32
+ *            scales [cols/128][rows]: the scale of the tile holding
+ *            x[r][128b .. 128b+127] is s[b*rows + r].  Scales are stored
+ *            k-block-major so that the 128 row scales of one GEMM tile are
+ *            contiguous.  Ignored (may be NULL) without the flag.
+ *   qT, sT : with FP8BS_COLWISE_T -- the 128x1-tiled payload written
+ *            transposed, qT [cols][rows] (qT[c][r] encodes x[r][c]), and
+ *            FP32 scales sT [rows/128][cols]: the scale of the tile holding
+ *            x[128b .. 128b+127][c] is sT[b*cols + c].  Ignored (may be NULL)
+ *            without the flag.
+ * rows is the token count M for X or dY; cols is K (for X) or N (for dY).
+ * Passage: the pages' fine-grained (tile-wise) activation quantization,
+ * "FP8：加快 RTX 5090 上的训练" and section 2.1 of the arXiv text.
+ */
+int fp8bs_quantize_act(const void* x, int64_t rows, int64_t cols, unsigned flags,
+                       uint8_t* q, float* s, uint8_t* qT, float* sT, void* stream);
+
+/*
+ * Weight quantization with 128x128 blocks.
+ *   w  : BF16 [n][k] (out features x in features), read only.
+ *   q  : E4M3 payload [n][k] (used by fprop).
+ *   qT : NULL, or E4M3 [k][n] holding the same bytes transposed (used by
+ *        dgrad, which contracts over n).  A 128x128 block's scale is the
+ *        same in both layouts.
+ *   s  : FP32 [n/128][k/128]; block (i, j) covers w[128i..][128j..].
+ * Passage: the pages' block-wise weight quantization (same sections).
+ */
+int fp8bs_quantize_weight(const void* w, int64_t n, int64_t k, uint8_t* q, uint8_t* qT,
+                          float* s, void* stream);
+
+/*
+ * Forward GEMM  Y = X W^T  (BF16 out [M][N]).
+ *   xq [M][K] E4M3 with sx [K/128][M] (from fp8bs_quantize_act, ROWWISE),
+ *   wq [N][K] E4M3 with sw [N/128][K/128] (from fp8bs_quantize_weight).
+ *   Y[m][n] = bf16( sum_b fma-chain of P_b[m][n] * (sx[b][m] * sw[n/128][b]) )
+ *   with P_b the FP32 tensor-core sum over k in [128b, 128b+128).
+ * Passage: "main linear-layer GEMMs on the FP8 path" (blog section
+ * "FP8：加快 RTX 5090 上的训练"; arXiv part 1/7, section 2.1).
+ */
+int fp8bs_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                     void* y, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Data-gradient GEMM  dX = dY W  (BF16 out [M][K]); contraction over N.
+ *   dyq [M][N] E4M3 with sdy [N/128][M] (fp8bs_quantize_act on dY, ROWWISE),
+ *   wqT [K][N] E4M3 (the transposed payload from fp8bs_quantize_weight),
+ *   sw  [N/128][K/128] (the same weight scales as fprop; block (b, k/128)
+ *       scales contraction block b of output column k).
+ * Passage: as for fprop (the backward linear GEMMs are on the FP8 path).
+ */
+int fp8bs_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw,
+                     void* dx, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Weight-gradient GEMM  dW = dY^T X  (BF16 out [N][K]); contraction over
+ * the M tokens.
+ *   dyTq [N][M] E4M3 with sdyT [M/128][N] (fp8bs_quantize_act on dY,
+ *        COLWISE_T), xTq [K][M] E4M3 with sxT [M/128][K] (the same on X).
+ *   dW[n][k] = bf16( fma-chain over token blocks b of
+ *              P_b[n][k] * (sdyT[b][n] * sxT[b][k]) ).
+ * Passage: as for fprop.
+ */
+int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
+                     void* dw, int64_t M, int64_t N, int64_t K, void* stream);
+
+/* Synchronizes `stream`, then returns and clears the current device's
+ * status word: FP8BS_OK, FP8BS_ERR_TIMEOUT (a kernel gave up a bounded
+ * wait and returned early; its outputs are undefined), or FP8BS_ERR_CUDA
+ * if the synchronization itself failed. */
+int fp8bs_get_device_status(void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* fp8bs_status_string(int status);
+
+/* Number of kernels launched by this process through the library (all
+ * entry points, all devices); a diagnostic counter. */
+int64_t fp8bs_launch_count(void);
+
+/*
+ * Test hooks (not for production use).
+ *   fp8bs_debug_set_wait_timeout_ns: the limit of every bounded device wait
+ *     (default 2e9 ns); 0 restores the default.
+ *   fp8bs_debug_set_fault: when 1, the next GEMM launch withholds one
+ *     operand copy so that the kernel's bounded wait expires and it reports
+ *     FP8BS_ERR_TIMEOUT without faulting; reset to 0 after that launch.
+ *   fp8bs_debug_e4m3_encode_bits: runs the kernels' FP32->E4M3 encoder on
+ *     the FP32 values whose bit patterns are first .. first+n-1, writing n
+ *     codes to the device buffer `out`.
+ */
+int fp8bs_debug_set_wait_timeout_ns(int64_t ns);
+int fp8bs_debug_set_fault(int mode);
+int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H_ */

@@ -228,13 +228,12 @@ void orc_quant_weight_128x128(const uint16_t* w, int64_t n, int64_t k,
 /* GEMMs with per-128-K promotion                                      */
 /* ------------------------------------------------------------------ */
 
+/* Decoded value of every E4M3 code, filled when the library is loaded (so
+ * concurrent callers on several threads only ever read it). */
 static double g_dec[256];
-static int g_dec_ready = 0;
 
-static void dec_init(void) {
-    if (g_dec_ready) return;
+__attribute__((constructor)) static void dec_table_init(void) {
     for (int c = 0; c < 256; c++) g_dec[c] = orc_e4m3_decode((uint8_t)c);
-    g_dec_ready = 1;
 }
 
 /* One output element of a block-scaled product.
@@ -284,7 +283,6 @@ void orc_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq,
                     const float* sw, int64_t M, int64_t N, int64_t K,
                     const int64_t* rows, int64_t nrows, float* out_f32,
                     uint16_t* out_bf16, double* out_sumabs) {
-    dec_init();
     int64_t kb = K / 128;
     for (int64_t i = 0; i < nrows; i++) {
         int64_t m = rows[i];
@@ -306,7 +304,6 @@ void orc_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wq,
                     const float* sw, int64_t M, int64_t N, int64_t K,
                     const int64_t* rows, int64_t nrows, float* out_f32,
                     uint16_t* out_bf16, double* out_sumabs) {
-    dec_init();
     int64_t kb = K / 128;
     uint8_t col[65536];
     if (N > 65536) return;
@@ -330,7 +327,6 @@ void orc_gemm_wgrad(const uint8_t* dytq, const float* sdyt, const uint8_t* xtq,
                     const float* sxt, int64_t M, int64_t N, int64_t K,
                     const int64_t* rows, int64_t nrows, float* out_f32,
                     uint16_t* out_bf16, double* out_sumabs) {
-    dec_init();
     for (int64_t i = 0; i < nrows; i++) {
         int64_t n = rows[i];
         for (int64_t k = 0; k < K; k++) {

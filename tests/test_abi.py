@@ -1,0 +1,86 @@
+"""The C ABI library loads without a GPU and exports every symbol that
+include/fp8bs.h declares; argument validation answers before any launch.
+(No call here reaches a kernel: every call fails validation first.)"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from fp8_block_scaled_16_b300 import binding as B
+from fp8_block_scaled_16_b300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8bs.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(fp8bs_\w+)\s*\(", text))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm_fprop", "fp8bs_gemm_dgrad",
+              "fp8bs_gemm_wgrad", "fp8bs_get_device_status", "fp8bs_status_string"):
+        assert n in names
+    assert names == set(B.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.check_output(["nm", "-D", "--defined-only", build_mod.LIB], text=True)
+    exported = set(re.findall(r"\bT (fp8bs_\w+)", out))
+    assert declared_functions() <= exported
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_library_needs_no_driver_to_load():
+    out = subprocess.check_output(["ldd", build_mod.LIB], text=True)
+    assert "libcuda.so" not in out  # the driver API is resolved at run time
+
+
+def test_status_strings(lib):
+    for code, name in B.STATUS.items():
+        assert B.fp8bs_status_string(code) == name
+    assert B.fp8bs_status_string(99) == "FP8BS_ERR_UNKNOWN"
+
+
+def test_validation_before_launch(lib):
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails validation
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.fp8bs_quantize_act(None, 128, 128, 1, fake, fake, None, None, None) == 1
+    assert lib.fp8bs_quantize_act(fake, 128, 128, 0, fake, fake, None, None, None) == 1
+    assert lib.fp8bs_quantize_act(fake, 128, 128, 4, fake, fake, None, None, None) == 1
+    assert lib.fp8bs_quantize_act(fake, 128, 128, 2, fake, fake, None, None, None) == 1  # qT/sT missing
+    assert lib.fp8bs_quantize_act(fake, 100, 128, 1, fake, fake, None, None, None) == 2
+    assert lib.fp8bs_quantize_act(fake, 128, -128, 1, fake, fake, None, None, None) == 2
+    assert lib.fp8bs_quantize_act(fake, 128 * 65536, 128, 1, fake, fake, None, None, None) == 2
+    assert lib.fp8bs_quantize_act(odd, 128, 128, 1, fake, fake, None, None, None) == 3
+    assert lib.fp8bs_quantize_weight(fake, 128, 128, None, None, fake, None) == 1
+    assert lib.fp8bs_quantize_weight(fake, 128, 130, fake, None, fake, None) == 2
+    assert lib.fp8bs_quantize_weight(fake, 128, 128, fake, odd, fake, None) == 3
+    for fn in (lib.fp8bs_gemm_fprop, lib.fp8bs_gemm_dgrad, lib.fp8bs_gemm_wgrad):
+        assert fn(fake, fake, None, fake, fake, 128, 128, 128, None) == 1
+        assert fn(fake, fake, fake, fake, fake, 128, 256, 0, None) == 2
+        assert fn(fake, fake, fake, fake, fake, 128, 200, 128, None) == 2
+        assert fn(fake, fake, fake, odd, fake, 128, 128, 128, None) == 3
+    assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, None, None) == 1
+    assert lib.fp8bs_debug_e4m3_encode_bits(0xFFFFFFF0, 32, fake, None) == 2
+    assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, odd, None) == 3
+
+
+def test_debug_setters(lib):
+    assert lib.fp8bs_debug_set_fault(2) == 1
+    assert lib.fp8bs_debug_set_fault(0) == 0
+    assert lib.fp8bs_debug_set_wait_timeout_ns(-1) == 1
+    assert lib.fp8bs_debug_set_wait_timeout_ns(0) == 0
+    assert lib.fp8bs_launch_count() >= 0

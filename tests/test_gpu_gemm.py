@@ -1,0 +1,184 @@
+"""GPU parity of the block-scaled GEMMs against the oracle, through the C ABI.
+
+Each case runs one linear layer's step on the GPU (quantize X, W, dY; fprop,
+dgrad, wgrad), checks every quantized operand bit-exactly against the
+oracle's, then checks the GEMM outputs against the oracle's unrounded FP32
+accumulators with the acceptance rule in tests/_parity.py: on every output
+for the small cases, and on 256 seeded random rows (randperm under seed + 1000)
+for the full-size workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_16_b300 import binding as B
+from fp8_block_scaled_16_b300 import inputs
+from fp8_block_scaled_16_b300.linear import Fp8LinearStep
+from tests._parity import assert_gemm_close, np_bf16_bits, np_f32, np_u8, oracle_gemm_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    B.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def same_bits(gpu: torch.Tensor, ref: np.ndarray, what: str):
+    g = np_u8(gpu) if gpu.dtype == torch.uint8 else np_f32(gpu).view(np.uint32)
+    r = ref if ref.dtype == np.uint8 else ref.view(np.uint32)
+    assert np.array_equal(g, r), f"{what} differs from the oracle"
+
+
+def check_linear(x, w, dy, ops, seed, sample=None):
+    """Run one linear's step on the GPU and compare everything with the
+    oracle.  sample=None checks every output row."""
+    M, K = x.shape
+    N = w.shape[0]
+    st = Fp8LinearStep(M, N, K, ops=ops)
+    y, dx, dw = st.step(x.cuda(), w.cuda(), dy.cuda() if dy is not None else None)
+    assert B.fp8bs_get_device_status() == 0
+    torch.cuda.synchronize()
+
+    oxq, osx = oracle.quant_rowwise_1x128(x)
+    owq, owqT, osw = oracle.quant_weight_128x128(w, want_t="dgrad" in ops)
+    same_bits(st.xq, oxq, "Xq")
+    same_bits(st.sx, osx, "sX")
+    same_bits(st.wq, owq, "Wq")
+    same_bits(st.sw, osw, "sW")
+
+    def rows_of(total):
+        if sample is None:
+            return np.arange(total)
+        return inputs.sample_rows(total, seed + 1000, sample).numpy()
+
+    worst = {}
+    r = rows_of(M)
+    acc, _, sab = oracle_gemm_rows("fprop", oxq, osx, owq, osw, r)
+    worst["fprop"] = assert_gemm_close(np_bf16_bits(y)[r], acc, sab, "fprop")
+    if "dgrad" in ops:
+        same_bits(st.wqT, owqT, "WqT")
+        odyq, osdy = oracle.quant_rowwise_1x128(dy)
+        same_bits(st.dyq, odyq, "dYq")
+        same_bits(st.sdy, osdy, "sdY")
+        acc, _, sab = oracle_gemm_rows("dgrad", odyq, osdy, owq, osw, r)
+        worst["dgrad"] = assert_gemm_close(np_bf16_bits(dx)[r], acc, sab, "dgrad")
+    if "wgrad" in ops:
+        oxTq, osxT = oracle.quant_colwise_128x1_T(x)
+        odyTq, osdyT = oracle.quant_colwise_128x1_T(dy)
+        same_bits(st.xTq, oxTq, "XTq")
+        same_bits(st.sxT, osxT, "sXT")
+        same_bits(st.dyTq, odyTq, "dYTq")
+        same_bits(st.sdyT, osdyT, "sdYT")
+        rn = rows_of(N)
+        acc, _, sab = oracle_gemm_rows("wgrad", odyTq, osdyT, oxTq, osxT, rn)
+        worst["wgrad"] = assert_gemm_close(np_bf16_bits(dw)[rn], acc, sab, "wgrad")
+    return worst
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 128, 128),      # one tile, one K block, N below the tile width
+    (384, 384, 640),      # ragged N tile (384 = 256 + 128), 5 K blocks
+    (256, 640, 384),      # dgrad output 384 wide: ragged; wgrad contracts 256 tokens
+    (1152, 1280, 1024),   # more tiles than a fraction of the SMs, several per CTA
+])
+def test_small_shapes_full_outputs(M, N, K):
+    seed = M * 7 + N * 3 + K
+    x = inputs.random_bf16((M, K), seed=seed)
+    x[:, K // 3] *= 40.0
+    w = inputs.random_bf16((N, K), seed=seed + 1, std=0.02)
+    dy = inputs.random_bf16((M, N), seed=seed + 2, std=1e-3)
+    check_linear(x, w, dy, ("fprop", "dgrad", "wgrad"), seed)
+
+
+def test_persistent_tail_more_tiles_than_sms():
+    # 148 SMs: 40 x 9 = 360 tiles of 128x256 -> every CTA loops, last wave partial.
+    M, N, K = 5120, 2304, 256
+    x = inputs.random_bf16((M, K), seed=5)
+    w = inputs.random_bf16((N, K), seed=6, std=0.02)
+    dy = inputs.random_bf16((M, N), seed=7, std=1e-3)
+    check_linear(x, w, dy, ("fprop", "dgrad", "wgrad"), 5, sample=256)
+
+
+def test_tiny_fprop_workload_full_output():
+    wl = inputs.WORKLOADS["tiny_fprop_256x512x512"]
+    d = inputs.make_linear_inputs(wl)[0]
+    check_linear(d["x"], d["w"], None, ("fprop",), wl.seed)
+
+
+@pytest.mark.parametrize("name", ["attn_qkv_fprop_8192x3072x2048", "mlp_gate_up_16384x11264x2048",
+                                  "mlp_down_16384x2048x5632"])
+def test_full_size_workloads_sampled_rows(name):
+    wl = inputs.WORKLOADS[name]
+    d = inputs.make_linear_inputs(wl)[0]
+    check_linear(d["x"], d["w"], d.get("dy"), wl.linears[0].ops, wl.seed, sample=256)
+
+
+def test_decoder_layer_workload_sampled_rows():
+    wl = inputs.WORKLOADS["decoder_layer_32768"]
+    for lin, d in zip(wl.linears, inputs.make_linear_inputs(wl)):
+        check_linear(d["x"], d["w"], d["dy"], lin.ops, wl.seed, sample=256)
+        torch.cuda.empty_cache()
+
+
+def test_zero_inputs_give_zero_outputs():
+    M, N, K = 256, 512, 256
+    st = Fp8LinearStep(M, N, K)
+    z = torch.zeros
+    y, dx, dw = st.step(z(M, K, dtype=torch.bfloat16, device="cuda"), z(N, K, dtype=torch.bfloat16, device="cuda"),
+                        z(M, N, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert not y.any() and not dx.any() and not dw.any()
+    assert torch.all(st.sx == 1.0) and torch.all(st.sw == 1.0)
+
+
+def test_deterministic():
+    M, N, K = 1024, 1536, 768
+    x = inputs.random_bf16((M, K), seed=11).cuda()
+    w = inputs.random_bf16((N, K), seed=12, std=0.02).cuda()
+    dy = inputs.random_bf16((M, N), seed=13, std=1e-3).cuda()
+    st = Fp8LinearStep(M, N, K)
+    a = [t.clone() for t in st.step(x, w, dy)]
+    b = [t.clone() for t in st.step(x, w, dy)]
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
+def test_bounded_wait_reports_timeout_and_gpu_stays_usable():
+    """A withheld operand copy makes one CTA's MMA wait run out: the kernel
+    records FP8BS_ERR_TIMEOUT and returns (no trap, no hang); the next
+    launch on the same context is correct."""
+    M, N, K = 512, 1024, 512
+    x = inputs.random_bf16((M, K), seed=21)
+    w = inputs.random_bf16((N, K), seed=22, std=0.02)
+    xq, sx, _, _ = B.fp8bs_quantize_act(x.cuda(), B.ROWWISE)
+    wq, _, sw = B.fp8bs_quantize_weight(w.cuda(), want_t=False)
+    assert B.fp8bs_get_device_status() == 0
+    try:
+        B.fp8bs_debug_set_wait_timeout_ns(50_000_000)
+        B.fp8bs_debug_set_fault(1)
+        B.fp8bs_gemm_fprop(xq, sx, wq, sw)
+        assert B.fp8bs_get_device_status() == 6  # FP8BS_ERR_TIMEOUT
+    finally:
+        B.fp8bs_debug_set_fault(0)
+        B.fp8bs_debug_set_wait_timeout_ns(0)
+    assert B.fp8bs_get_device_status() == 0
+    y = B.fp8bs_gemm_fprop(xq, sx, wq, sw)
+    assert B.fp8bs_get_device_status() == 0
+    oxq, osx = oracle.quant_rowwise_1x128(x)
+    owq, _, osw = oracle.quant_weight_128x128(w, want_t=False)
+    acc, _, sab = oracle_gemm_rows("fprop", oxq, osx, owq, osw, np.arange(M))
+    assert_gemm_close(np_bf16_bits(y), acc, sab, "fprop after timeout")
+
+
+def test_rejects_bad_arguments():
+    lib = B.load()
+    t = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    p = t.data_ptr()
+    assert lib.fp8bs_gemm_fprop(None, p, p, p, p, 128, 128, 128, None) == 1
+    assert lib.fp8bs_gemm_fprop(p, p, p, p, p, 100, 128, 128, None) == 2
+    assert lib.fp8bs_gemm_wgrad(p, p, p, p, p, 128, 0, 128, None) == 2
+    assert lib.fp8bs_gemm_dgrad(p + 8, p, p, p, p, 128, 128, 128, None) == 3

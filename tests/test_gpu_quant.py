@@ -1,0 +1,147 @@
+"""GPU parity of the quantizers against the oracle: payload bytes and scales
+must be bit-identical, through the C ABI."""
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_16_b300 import binding as B
+from fp8_block_scaled_16_b300 import inputs
+from tests._parity import THREADS, np_f32, np_u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    B.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def check_rowwise(x: torch.Tensor):
+    q, s, _, _ = B.fp8bs_quantize_act(x.cuda(), B.ROWWISE)
+    oq, os_ = oracle.quant_rowwise_1x128(x)
+    assert np.array_equal(np_u8(q), oq), "1x128 payload differs"
+    assert np.array_equal(np_f32(s).view(np.uint32), os_.view(np.uint32)), "1x128 scales differ"
+
+
+def check_colwise(x: torch.Tensor, fused: bool):
+    flags = B.COLWISE_T | (B.ROWWISE if fused else 0)
+    q, s, qT, sT = B.fp8bs_quantize_act(x.cuda(), flags)
+    oqT, osT = oracle.quant_colwise_128x1_T(x)
+    assert np.array_equal(np_u8(qT), oqT), "128x1 transposed payload differs"
+    assert np.array_equal(np_f32(sT).view(np.uint32), osT.view(np.uint32)), "128x1 scales differ"
+    if fused:
+        oq, os_ = oracle.quant_rowwise_1x128(x)
+        assert np.array_equal(np_u8(q), oq)
+        assert np.array_equal(np_f32(s).view(np.uint32), os_.view(np.uint32))
+
+
+def check_weight(w: torch.Tensor):
+    q, qT, s = B.fp8bs_quantize_weight(w.cuda())
+    oq, oqT, os_ = oracle.quant_weight_128x128(w)
+    assert np.array_equal(np_u8(q), oq), "weight payload differs"
+    assert np.array_equal(np_u8(qT), oqT), "transposed weight payload differs"
+    assert np.array_equal(np_f32(s).view(np.uint32), os_.view(np.uint32)), "weight scales differ"
+    q2, none, s2 = B.fp8bs_quantize_weight(w.cuda(), want_t=False)
+    assert none is None and torch.equal(q2, q) and torch.equal(s2, s)
+
+
+def test_encoder_matches_oracle_on_all_fp32_patterns():
+    """The kernels' FP32->E4M3 conversion against the oracle's hand-written
+    encoder on all 2^32 bit patterns (NaNs compared as 'any NaN code')."""
+    chunk = 1 << 28
+    out = torch.empty(chunk, dtype=torch.uint8, device="cuda")
+    for c in range(16):
+        first = c * chunk
+        B.fp8bs_debug_e4m3_encode_bits(first, chunk, out)
+        gpu = np_u8(out)
+        parts = np.array_split(np.arange(chunk, dtype=np.int64), THREADS)
+        with ThreadPoolExecutor(THREADS) as ex:
+            ref = np.concatenate(list(ex.map(lambda p: oracle.e4m3_encode_bits(first + int(p[0]), p.size), parts)))
+        bits = np.arange(chunk, dtype=np.uint32) + np.uint32(first)
+        nan_in = (bits & 0x7FFFFFFF) > 0x7F800000
+        same = gpu == ref
+        same |= nan_in & ((gpu & 0x7F) == 0x7F) & ((ref & 0x7F) == 0x7F)
+        if not same.all():
+            i = int(np.argmin(same))
+            raise AssertionError(f"pattern {int(bits[i]):#010x}: gpu {int(gpu[i]):#04x} oracle {int(ref[i]):#04x}")
+
+
+def test_rowwise_small_shapes_and_edge_tiles():
+    x = inputs.random_bf16((384, 640), seed=101)
+    x[0, :128] = 0.0                       # all-zero tile
+    x[1, 128:256] = -0.0                   # all negative-zero tile
+    x[2, :128] = 0.0
+    x[2, 7] = -(2.0 ** -133)               # amax: smallest BF16 subnormal
+    x[3, 256:384] *= 1e30                  # huge values
+    x[4, 384:512] *= 1e-38                 # subnormal-scale values
+    x[5, 5] = 3.0e38                       # near BF16 max
+    x[6, :] = 448.0                        # constant tile
+    x[:, 300] *= 60.0                      # outlier channel
+    check_rowwise(x)
+
+
+def test_colwise_and_fused_small_shapes_and_edge_tiles():
+    x = inputs.random_bf16((384, 640), seed=102)
+    x[:128, 0] = 0.0
+    x[128:256, 1] = -0.0
+    x[:128, 2] = 0.0
+    x[77, 2] = 2.0 ** -133
+    x[:, 3] *= 1e30
+    x[:, 600] *= 1e-38
+    x[300, :] *= 50.0
+    check_colwise(x, fused=False)
+    check_colwise(x, fused=True)
+
+
+def test_weight_small_shapes_and_edge_blocks():
+    w = inputs.random_bf16((384, 640), seed=103, std=0.02)
+    w[:128, :128] = 0.0
+    w[128:256, 128:256] *= 1e-36
+    w[300, 600] = 5.0
+    check_weight(w)
+
+
+def test_tiny_fprop_workload_quantizers():
+    d = inputs.make_linear_inputs(inputs.WORKLOADS["tiny_fprop_256x512x512"])[0]
+    check_rowwise(d["x"])
+    check_colwise(d["x"], fused=True)
+    check_weight(d["w"])
+
+
+@pytest.mark.parametrize("name", ["attn_qkv_fprop_8192x3072x2048", "mlp_gate_up_16384x11264x2048",
+                                  "mlp_down_16384x2048x5632"])
+def test_full_size_workload_quantizers(name):
+    wl = inputs.WORKLOADS[name]
+    d = inputs.make_linear_inputs(wl)[0]
+    lin = wl.linears[0]
+    if "wgrad" in lin.ops:
+        check_colwise(d["x"], fused=True)
+    else:
+        check_rowwise(d["x"])
+    check_weight(d["w"])
+    if "dy" in d:
+        if "wgrad" in lin.ops:
+            check_colwise(d["dy"], fused=True)
+        else:
+            check_rowwise(d["dy"])
+
+
+def test_deterministic_and_rejects_bad_arguments():
+    x = inputs.random_bf16((256, 256), seed=104).cuda()
+    a = B.fp8bs_quantize_act(x, B.ROWWISE | B.COLWISE_T)
+    b = B.fp8bs_quantize_act(x, B.ROWWISE | B.COLWISE_T)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    with pytest.raises(B.Fp8bsError) as e:
+        B.fp8bs_quantize_act(inputs.random_bf16((256, 200), seed=1).cuda(), B.ROWWISE)
+    assert e.value.status == 2
+    lib = B.load()
+    assert lib.fp8bs_quantize_act(x.data_ptr() + 2, 256, 256, 1, a[0].data_ptr(), a[1].data_ptr(),
+                                  None, None, None) == 3
+    assert lib.fp8bs_quantize_act(x.data_ptr(), 256, 256, 0, None, None, None, None, None) == 1
