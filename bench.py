@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark: one training step of the FP8 block-scaled linear layers of a
+decoder layer on B300, through the library's C ABI.
+
+A step is one pass of the whole path over one batch: for each linear,
+quantize X (1x128 row-wise and 128x1 transposed in one read), quantize W
+(128x128 blocks plus the transposed copy), fprop, quantize dY (both
+layouts), dgrad, wgrad.  The default workload is one decoder layer's four
+linears at 32768 tokens (QKV 2048->3072, O 2048->2048, gate+up
+2048->11264, down 5632->2048), synthetic inputs as in
+fp8_block_scaled_16_b300/inputs.py.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is GEMM TFLOP/s of the whole step
+(all GEMM FLOPs of all ranks / the slowest rank's step time, quantizers
+included in the time).  `--impl reference` times the CPU oracle on a bounded
+sample of the same workload instead.  With N > 1 (torchrun) the ranks are
+independent replicas (weak scaling): the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fp8_block_scaled_16_b300 import dist as D  # noqa: E402
+from fp8_block_scaled_16_b300 import inputs  # noqa: E402
+
+METRIC = "FP8 block-scaled GEMM TFLOPS fprop/dgrad/wgrad, % of B300 FP8 peak; quant GB/s"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "decoder_layer_32768"
+SWEEP_WORKLOADS = ("attn_qkv_fprop_8192x3072x2048", "mlp_gate_up_16384x11264x2048", "mlp_down_16384x2048x5632")
+FP8_PER_BF16 = 4.5 / 2.25        # nominal dense FP8 : BF16 tensor rate
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons every 20 ms while running."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
+        "sync_boost": 0x10, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80, "display_clock_setting": 0x100,
+    }
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+
+    def start(self):
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            h = pynvml.nvmlDeviceGetHandleByIndex(self.idx)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self._nvml = (pynvml, h)
+        except Exception:
+            self._nvml = None
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                if self._nvml:
+                    pynvml, h = self._nvml
+                    mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                    reasons = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                    self.samples.append((mhz, reasons))
+                else:
+                    out = subprocess.check_output(
+                        ["nvidia-smi", "-i", str(self.idx), "--query-gpu=clocks.sm,clocks.max.sm",
+                         "--format=csv,noheader,nounits"], text=True)
+                    a, b = [int(v) for v in out.strip().split(",")]
+                    self.max_mhz = b
+                    self.samples.append((a, 0))
+            except Exception:
+                pass
+            self._stop.wait(0.02)
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join()
+        seen = 0
+        for _, r in self.samples:
+            seen |= r
+        names = sorted(n for n, bit in self.REASONS.items() if seen & bit)
+        mhz = [m for m, _ in self.samples]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def time_step(launch_lists, steps, per_launch):
+    """Runs `steps` steps on the current stream; returns total ms and, if
+    per_launch, the ms of every launch (CUDA events between launches)."""
+    flat = [l for ll in launch_lists for l in ll]
+    st = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = []
+    t0.record(st)
+    for _ in range(steps):
+        if per_launch:
+            prev = torch.cuda.Event(enable_timing=True)
+            prev.record(st)
+            for l in flat:
+                l.run()
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(st)
+                marks.append((l, prev, ev))
+                prev = ev
+        else:
+            for l in flat:
+                l.run()
+    t1.record(st)
+    torch.cuda.synchronize()
+    per = [(l, a.elapsed_time(b)) for l, a, b in marks]
+    return t0.elapsed_time(t1), per
+
+
+def summarize(per):
+    agg = {}
+    for l, ms in per:
+        a = agg.setdefault(l.op, {"launches": 0, "ms": 0.0, "work": 0, "unit": l.unit})
+        a["launches"] += 1
+        a["ms"] += ms
+        a["work"] += l.work
+    return agg
+
+
+def op_rate(a):
+    if a["unit"] == "flops":
+        return a["work"] / (a["ms"] * 1e-3) / 1e12, "TFLOP/s"
+    return a["work"] / (a["ms"] * 1e-3) / 1e9, "GB/s"
+
+
+def flush_l2(buf):
+    buf.add_(1)  # writes 512 MiB, far more than the 126 MB L2
+
+
+def sweep(peaks, fp8_peak):
+    """Per-kernel rates on the single-linear workloads (each launch timed
+    alone with events, L2 flushed before it, median of 10)."""
+    from fp8_block_scaled_16_b300.linear import Fp8LinearStep
+
+    res = {}
+    flush = torch.zeros(128 << 20, dtype=torch.float32, device="cuda")
+    for name in SWEEP_WORKLOADS:
+        wl = inputs.WORKLOADS[name]
+        lin = wl.linears[0]
+        d = inputs.make_linear_inputs(wl, device="cuda")[0]
+        st = Fp8LinearStep(lin.tokens, lin.out_features, lin.in_features, ops=lin.ops)
+        ll = st.launch_list(d["x"], d["w"], d.get("dy"))
+        for l in ll:
+            l.run()
+        torch.cuda.synchronize()
+        out = {}
+        for i, l in enumerate(ll):
+            times = []
+            for _ in range(10):
+                flush_l2(flush)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                l.run()
+                b.record()
+                b.synchronize()
+                times.append(a.elapsed_time(b))
+            ms = statistics.median(times)
+            key = l.op if l.op != "quant_act" else ("quant_x" if i == 0 else "quant_dy")
+            if l.unit == "flops":
+                tf = l.work / (ms * 1e-3) / 1e12
+                out[key] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 3)}
+            else:
+                gbs = l.work / (ms * 1e-3) / 1e9
+                out[key] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)}
+        res[name] = out
+        del st, d, ll
+        torch.cuda.empty_cache()
+    return res
+
+
+def e2e_run(wl, steps_data, steps):
+    """Same step through the public API with inputs copied from pinned host
+    memory and results copied back every step."""
+    from fp8_block_scaled_16_b300.linear import Fp8LinearStep  # noqa: F401
+
+    host_in, host_out, dev, h2d, d2h = [], [], [], 0, 0
+    for st, d in steps_data:
+        hi = {k: v.cpu().pin_memory() for k, v in d.items()}
+        host_in.append(hi)
+        h2d += sum(v.numel() * v.element_size() for v in hi.values())
+        outs = [t for t in (st.y, st.dx, st.dw) if t is not None]
+        ho = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        host_out.append((outs, ho))
+        d2h += sum(t.numel() * t.element_size() for t in outs)
+        dev.append({k: torch.empty_like(v) for k, v in d.items()})
+    s = torch.cuda.current_stream()
+    lls = [st.launch_list(dv["x"], dv["w"], dv.get("dy")) for (st, _), dv in zip(steps_data, dev)]
+
+    def one():
+        for hi, dv, ll, (outs, ho) in zip(host_in, dev, lls, host_out):
+            for k in hi:
+                dv[k].copy_(hi[k], non_blocking=True)
+            for l in ll:
+                l.run()
+            for t, h in zip(outs, ho):
+                h.copy_(t, non_blocking=True)
+        s.synchronize()  # the host reads the step's results
+
+    one()
+    t = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = (time.perf_counter() - t) / steps
+    return dt, h2d, d2h
+
+
+def cpu_sample(lin_data, rows):
+    """The oracle (single-threaded C) on a bounded sample of the step: for
+    each linear, the first 128 tokens quantized both ways and W quantized in
+    full, then `rows` rows of fprop and dgrad and `rows` rows of wgrad over
+    that token block.  Returns (flops, seconds)."""
+    import numpy as np
+
+    import oracle
+
+    flops, t = 0, time.perf_counter()
+    for lin, d in lin_data:
+        x = d["x"][:128].cpu()
+        w = d["w"].cpu()
+        N, K = w.shape
+        r = np.arange(rows)
+        xq, sx = oracle.quant_rowwise_1x128(x)
+        wq, _, sw = oracle.quant_weight_128x128(w, want_t=False)
+        oracle.gemm_fprop(xq, sx, wq, sw, rows=r)
+        flops += 2 * rows * N * K
+        if "dgrad" in lin.ops:
+            dy = d["dy"][:128].cpu()
+            dyq, sdy = oracle.quant_rowwise_1x128(dy)
+            oracle.gemm_dgrad(dyq, sdy, wq, sw, rows=r)
+            flops += 2 * rows * N * K
+        if "wgrad" in lin.ops:
+            dy = d["dy"][:128].cpu()
+            xTq, sxT = oracle.quant_colwise_128x1_T(x)
+            dyTq, sdyT = oracle.quant_colwise_128x1_T(dy)
+            oracle.gemm_wgrad(dyTq, sdyT, xTq, sxT, rows=r)
+            flops += 2 * rows * K * 128
+    return flops, time.perf_counter() - t
+
+
+def run_ours(args):
+    from fp8_block_scaled_16_b300 import binding as B
+    from fp8_block_scaled_16_b300.linear import Fp8LinearStep
+
+    ranks = D.init_from_env("nccl")
+    torch.cuda.set_device(ranks.local_rank)
+    device = torch.device("cuda", ranks.local_rank)
+    B.load()
+    peaks, peak_src = load_peaks()
+    fp8_burst = peaks["bf16_tflops"] * FP8_PER_BF16
+    fp8_sust = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+
+    wl = inputs.WORKLOADS[args.workload]
+    data = inputs.make_linear_inputs(wl, device="cuda")
+    steps_data = []
+    for lin, d in zip(wl.linears, data):
+        steps_data.append((Fp8LinearStep(lin.tokens, lin.out_features, lin.in_features, ops=lin.ops), d))
+    lls = [st.launch_list(d["x"], d["w"], d.get("dy")) for st, d in steps_data]
+    flops_step = sum(l.work for ll in lls for l in ll if l.unit == "flops")
+    launches_step = sum(len(ll) for ll in lls)
+    in_bytes = sum(v.numel() * v.element_size() for _, d in steps_data for v in d.values())
+
+    time_step(lls, args.warmup, per_launch=False)
+    assert B.fp8bs_get_device_status() == 0, "device status after warm-up"
+    count0 = B.fp8bs_launch_count()
+    D.barrier(ranks, device)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    total_ms, per = time_step(lls, args.steps, per_launch=True)
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    D.barrier(ranks, device)
+    launched = B.fp8bs_launch_count() - count0
+    status = B.fp8bs_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {B.fp8bs_status_string(status)}")
+
+    ms_step = total_ms / args.steps
+    ms_max = D.max_over_ranks(ranks, ms_step, device)
+    value = flops_step * ranks.world / (ms_max * 1e-3) / 1e12
+
+    agg = summarize(per)
+    dom_op = max(agg, key=lambda k: agg[k]["ms"])
+    a = agg[dom_op]
+    rate, runit = op_rate(a)
+    long_region = total_ms >= 2000.0
+    if a["unit"] == "flops":
+        peak = fp8_sust if long_region else fp8_burst
+        roof = {"bound": "tensor", "kernel": dom_op, "achieved": round(rate, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(rate / peak, 4), "traffic": None,
+                "peak_note": (f"FP8 = {'sustained' if long_region else 'burst'} bf16 cuBLAS "
+                              f"x {FP8_PER_BF16:g} (nominal FP8:BF16), {peak_src}")}
+    else:
+        roof = {"bound": "hbm", "kernel": dom_op, "achieved": round(rate, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(rate / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_note": f"STREAM-style copy, {peak_src}"}
+    breakdown = {}
+    for op, s in sorted(agg.items()):
+        r, u = op_rate(s)
+        frac = r / (fp8_burst if u == "TFLOP/s" else peaks["hbm_gbs"])
+        breakdown[op] = {"launches": s["launches"] // args.steps, "ms_per_step": round(s["ms"] / args.steps, 4),
+                         u: round(r, 1), "frac": round(frac, 3)}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ranks.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": wl.linears[0].tokens,
+                   "linears": [f"{l.name} {l.in_features}->{l.out_features}" for l in wl.linears],
+                   "step": "quant X (1x128+128x1T), quant W (128x128+T), fprop, quant dY (1x128+128x1T), "
+                           "dgrad, wgrad per linear",
+                   "gemm_tflop_per_step": round(flops_step / 1e12, 4),
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of BF16 inputs per step, L2 126 MB)",
+                   "inputs": "drawn on the GPU with torch's CUDA generator (recipe in inputs.py)",
+                   "parallelism": f"replicas x{ranks.world}" if ranks.world > 1 else "single GPU"},
+        "roofline": roof, "breakdown": breakdown, "gpu_launches": launched,
+        "gpu_launches_expected": launches_step * args.steps, "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        e2e_steps = max(1, min(args.steps, 3))
+        dt, h2d, d2h = e2e_run(wl, steps_data, e2e_steps)
+        dt_max = D.max_over_ranks(ranks, dt, device)
+        result["e2e"] = {"value": round(flops_step * ranks.world / dt_max / 1e12, 2), "unit": UNIT,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "ms_per_step": round(dt_max * 1e3, 2),
+                         "note": "pinned host inputs copied in and results copied out every step, via the "
+                                 "Python binding of the C ABI"}
+    if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu:
+        rows = args.cpu_rows
+        fl, sec = cpu_sample(list(zip(wl.linears, data)), rows)
+        result["cpu_baseline"] = {
+            "value": fl / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first 128 tokens of each linear quantized both ways, W quantized in full, {rows} rows of "
+                      f"fprop, dgrad and wgrad per linear; single-threaded C oracle, {sec:.1f} s"}
+    if ranks.world == 1 and not args.no_sweep:
+        result["per_workload"] = sweep(peaks, fp8_burst)
+    if ranks.rank == 0:
+        print(json.dumps(result), flush=True)
+    D.shutdown(ranks)
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    ranks = D.Ranks(int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0, False)
+    if ranks.rank != 0:
+        return
+    wl = inputs.WORKLOADS[args.workload]
+    data = inputs.make_linear_inputs(wl, device="cpu")
+    lin_data = list(zip(wl.linears, data))
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        cpu_sample(lin_data, rows)
+    fl = sec = 0.0
+    for _ in range(args.steps):
+        f, s = cpu_sample(lin_data, rows)
+        fl += f
+        sec += s
+    value = fl / sec / 1e12
+    sample = (f"first 128 tokens of each linear quantized both ways, W quantized in full, {rows} rows of fprop, "
+              f"dgrad and wgrad per linear; single-threaded C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 partial sums, f32 promotion",
+        "data": "synthetic", "config": {"workload": wl.name, "parallelism": "single host thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

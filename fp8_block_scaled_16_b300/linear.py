@@ -14,11 +14,20 @@ here; a trainer that keeps W fixed across micro-batches may quantize it once.
 """
 from __future__ import annotations
 
-from typing import Optional
+from dataclasses import dataclass
+from typing import Callable, List
 
 import torch
 
 from . import binding as B
+
+
+@dataclass
+class Launch:
+    op: str        # "quant_act", "quant_weight", "fprop", "dgrad", "wgrad"
+    work: int      # algorithmic FLOPs (GEMMs) or bytes (quantizers)
+    unit: str      # "flops" or "bytes"
+    run: Callable[[], object]
 
 
 class Fp8LinearStep:
@@ -42,32 +51,43 @@ class Fp8LinearStep:
         self.dw = e((N, K), bf) if "wgrad" in self.ops else None
         self.has_bwd = bwd
 
-    def launches_per_step(self) -> int:
-        n = 3  # quantize X, quantize W, fprop
+    def launch_list(self, x, w, dy=None, stream=None) -> List[Launch]:
+        """The step's library calls in order, each with its algorithmic work:
+        FLOPs (2 M N K) for a GEMM, bytes moved for a quantizer (BF16 read,
+        E4M3 written per requested layout, 4 bytes per scale)."""
+        M, N, K = self.M, self.N, self.K
+        wgrad, dgrad = "wgrad" in self.ops, "dgrad" in self.ops
+        xflags = B.ROWWISE | (B.COLWISE_T if wgrad else 0)
+        dyflags = (B.ROWWISE if dgrad else 0) | (B.COLWISE_T if wgrad else 0)
+
+        def act_bytes(rows, cols, flags):
+            n = rows * cols
+            layouts = bin(flags).count("1")
+            return 2 * n + layouts * (n + 4 * n // 128)
+
+        out = [
+            Launch("quant_act", act_bytes(M, K, xflags), "bytes",
+                   lambda: B.fp8bs_quantize_act(x, xflags, self.xq, self.sx, self.xTq, self.sxT, stream=stream)),
+            Launch("quant_weight", 2 * N * K + N * K * (2 if dgrad else 1) + 4 * (N // 128) * (K // 128), "bytes",
+                   lambda: B.fp8bs_quantize_weight(w, self.wq, self.wqT, self.sw, want_t=dgrad, stream=stream)),
+            Launch("fprop", 2 * M * N * K, "flops",
+                   lambda: B.fp8bs_gemm_fprop(self.xq, self.sx, self.wq, self.sw, self.y, stream=stream)),
+        ]
         if self.has_bwd:
-            n += 1  # quantize dY
-        n += ("dgrad" in self.ops) + ("wgrad" in self.ops)
-        return n
-
-    def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
-        flags = B.ROWWISE | (B.COLWISE_T if "wgrad" in self.ops else 0)
-        B.fp8bs_quantize_act(x, flags, self.xq, self.sx, self.xTq, self.sxT, stream=stream)
-        B.fp8bs_quantize_weight(w, self.wq, self.wqT, self.sw, want_t="dgrad" in self.ops, stream=stream)
-        return B.fp8bs_gemm_fprop(self.xq, self.sx, self.wq, self.sw, self.y, stream=stream)
-
-    def backward(self, dy: Optional[torch.Tensor], stream=None):
-        if not self.has_bwd:
-            return None, None
-        flags = (B.ROWWISE if "dgrad" in self.ops else 0) | (B.COLWISE_T if "wgrad" in self.ops else 0)
-        B.fp8bs_quantize_act(dy, flags, self.dyq, self.sdy, self.dyTq, self.sdyT, stream=stream)
-        dx = dw = None
-        if "dgrad" in self.ops:
-            dx = B.fp8bs_gemm_dgrad(self.dyq, self.sdy, self.wqT, self.sw, self.dx, stream=stream)
-        if "wgrad" in self.ops:
-            dw = B.fp8bs_gemm_wgrad(self.dyTq, self.sdyT, self.xTq, self.sxT, self.dw, stream=stream)
-        return dx, dw
+            out.append(Launch("quant_act", act_bytes(M, N, dyflags), "bytes",
+                              lambda: B.fp8bs_quantize_act(dy, dyflags, self.dyq, self.sdy, self.dyTq, self.sdyT,
+                                                           stream=stream)))
+        if dgrad:
+            out.append(Launch("dgrad", 2 * M * N * K, "flops",
+                              lambda: B.fp8bs_gemm_dgrad(self.dyq, self.sdy, self.wqT, self.sw, self.dx,
+                                                         stream=stream)))
+        if wgrad:
+            out.append(Launch("wgrad", 2 * M * N * K, "flops",
+                              lambda: B.fp8bs_gemm_wgrad(self.dyTq, self.sdyT, self.xTq, self.sxT, self.dw,
+                                                         stream=stream)))
+        return out
 
     def step(self, x, w, dy=None, stream=None):
-        y = self.forward(x, w, stream=stream)
-        dx, dw = self.backward(dy, stream=stream)
-        return y, dx, dw
+        for launch in self.launch_list(x, w, dy, stream=stream):
+            launch.run()
+        return self.y, self.dx, self.dw
