@@ -110,36 +110,25 @@ int launch_status() {
     return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
-// C[rows][cols] = block-scaled A[rows][kc] * B[cols][kc]^T (see gemm.cuh).
-int run_gemm(int sbmode, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
-             const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
-             cudaStream_t st) {
+template <int SBMODE, int BN>
+int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
+                const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
+                cudaStream_t st) {
     using namespace gemm;
-    DeviceInfo* d = nullptr;
-    int rc = current_device(&d);
-    if (rc != FP8BS_OK) return rc;
-
-    CUtensorMap tmA, tmB, tmSA, tmSB;
-    const uint64_t kblocks = static_cast<uint64_t>(kc / BK);
+    using T = Tile<BN>;
+    CUtensorMap tmA, tmB;
     if (!tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kc, rows, kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kc, cols, kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tmap_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sa, rows, kblocks, rows * 4, SA_FLOATS, 1,
-                 CU_TENSOR_MAP_SWIZZLE_NONE))
+        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kc, cols, kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return FP8BS_ERR_LAUNCH;
-    if (sbmode == SB_VECTOR) {
-        if (!tmap_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sb, cols, kblocks, cols * 4, SB_FLOATS, 1,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
-            return FP8BS_ERR_LAUNCH;
-    } else {
-        tmSB = tmSA;
-    }
 
     Params p;
     p.m_tiles = static_cast<int32_t>(rows / BM);
     p.n_tiles = static_cast<int32_t>((cols + BN - 1) / BN);
-    p.kblocks = static_cast<int32_t>(kblocks);
+    p.kblocks = static_cast<int32_t>(kc / BK);
     p.nb_valid = static_cast<int32_t>(cols / 128);
+    p.rows = rows;
     p.cols = cols;
+    p.sa = sa;
     p.sb = sb;
     p.sb_stride_j = sb_stride_j;
     p.sb_stride_b = sb_stride_b;
@@ -152,15 +141,27 @@ int run_gemm(int sbmode, const uint8_t* A, const uint8_t* B, int64_t rows, int64
     if (tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
     const int grid = static_cast<int>(tiles < d->sm_count ? tiles : d->sm_count);
 
-    auto kern = (sbmode == SB_VECTOR) ? gemm_kernel<SB_VECTOR> : gemm_kernel<SB_SCALAR>;
-    if (!d->gemm_attr_set[sbmode]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+    auto kern = gemm_kernel<SBMODE, BN>;
+    if (!d->gemm_attr_set[SBMODE]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
             return launch_status();
-        d->gemm_attr_set[sbmode] = true;
+        d->gemm_attr_set[SBMODE] = true;
     }
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmSA, tmSB, p);
+    kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(tmA, tmB, p);
     g_launches.fetch_add(1);
     return launch_status();
+}
+
+// C[rows][cols] = block-scaled A[rows][kc] * B[cols][kc]^T (see gemm.cuh).
+int run_gemm(int sbmode, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
+             const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
+             cudaStream_t st) {
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    if (sbmode == gemm::SB_VECTOR)
+        return launch_gemm<gemm::SB_VECTOR, 256>(d, A, B, rows, cols, kc, sa, sb, sb_stride_j, sb_stride_b, out, st);
+    return launch_gemm<gemm::SB_SCALAR, 256>(d, A, B, rows, cols, kc, sa, sb, sb_stride_j, sb_stride_b, out, st);
 }
 
 }  // namespace

@@ -10,24 +10,31 @@
 // follow prescribes (blog section "FP8：加快 RTX 5090 上的训练"; arXiv part
 // 1/7, section 2.1).
 //
-// Persistent kernel, one 384-thread CTA per SM, 128x256 output tiles:
-//   warp 0 (one lane): TMA producer -- A tile 128x128 B and B tile 256x128 B
-//       per K block into a STAGES-deep shared-memory ring (128-byte
-//       swizzle), plus the K block's row scales (and, for the weight
-//       gradient, its 256 column scales) into a separate scale ring;
+// Persistent kernel, one 384-thread CTA per SM, 128 x BN output tiles
+// (BN = 256), K block 128:
+//   warp 0 (one lane): TMA producer -- A tile 128x128 B and B tile BNx128 B
+//       per K block into a shared-memory ring (128-byte swizzle);
 //   warp 1 (one lane): MMA issuer -- four tcgen05.mma (K = 32 each) per K
-//       block into one of two 128x256 FP32 TMEM buffers (512 columns), the
-//       first with accumulate off, then commits to free the smem stage and
-//       to publish the buffer;
-//   warps 2, 3: idle (they complete the first warpgroup, whose registers
-//       are handed to the epilogue warpgroups with setmaxnreg);
+//       block into one of two 128 x BN FP32 TMEM buffers (all 512 columns),
+//       the first with accumulate off, then commits to free the smem stage
+//       and to publish the buffer;
+//   warp 2: scale loader -- per K block the 128 row scales (and, for the
+//       weight gradient, the BN column scales) into an 8-slot shared-memory
+//       ring with cp.async, one 16-byte copy per lane;
+//   warp 3: idle (it completes the first warpgroup, whose registers are
+//       handed to the epilogue warpgroups with setmaxnreg);
 //   warps 4..11: promotion + epilogue -- each warp owns a 32-lane TMEM
-//       quadrant (rows) and one 128-column half; per K block it loads its
-//       32x128 partial with tcgen05.ld, releases the buffer, and does
-//       acc = fma(P_b, sa*sb, acc) on 128 FP32 registers per thread; at the
-//       end of a tile it rounds to BF16 and stores.
+//       quadrant (rows) and one BN/2-column half; per K block it loads its
+//       partial with tcgen05.ld two 32-column chunks at a time, releases the
+//       TMEM buffer after the last load, and does acc = fma(P_b, sa*sb, acc)
+//       with packed FP32 FMAs on BN/2 registers per thread; at the end of a
+//       tile it rounds to BF16 and stores.
 // While the epilogue promotes block b, the tensor cores already compute
 // block b+1 into the other buffer.
+//
+// The scale ring is written with cp.async (generic proxy) rather than TMA:
+// the epilogue reads it with ordinary loads, and a TMA write into a slot
+// those loads have just released would need a proxy fence per K block.
 //
 // Every mbarrier wait is bounded (see WaitCtx): on expiry the CTA records
 // a timeout in the device status word, waits (bounded) for its own copies
@@ -41,15 +48,8 @@
 namespace fp8bs {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int STAGES = 4;
+constexpr int BM = 128, BK = 128;
 constexpr int SSLOTS = 8;
-constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SA_FLOATS = BM;
-constexpr int SB_FLOATS = BN;
-constexpr int SLOT_FLOATS = SA_FLOATS + SB_FLOATS;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 128 + NUM_EPI_WARPS * 32;
 // Register split after launch (launch: 168 per thread = 384 x 168 total).
@@ -58,41 +58,57 @@ constexpr int THREADS = 128 + NUM_EPI_WARPS * 32;
 // 128 x 48 + 256 x 224 = 63488 <= 64512.
 constexpr int REGS_CTRL = 48;
 constexpr int REGS_EPI = 224;
-constexpr uint32_t TMEM_COLS = 2 * BN;
-
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_SCALE = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_BAR = OFF_SCALE + SSLOTS * SLOT_FLOATS * 4;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * SSLOTS;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
-
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+constexpr uint32_t TMEM_COLS = 512;
 static_assert(THREADS == 384, "warp roles");
 static_assert(128 * REGS_CTRL + NUM_EPI_WARPS * 32 * REGS_EPI <= THREADS * 168, "register split");
 
 enum : int { SB_SCALAR = 0, SB_VECTOR = 1 };
 
+// Shared-memory plan for a 128 x BN tile.
+template <int BN>
+struct Tile {
+    static_assert(BN == 256, "tile width");
+    static constexpr int NBUF = static_cast<int>(TMEM_COLS) / BN;  // TMEM accumulator buffers
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;    // 4
+    static constexpr int SA_FLOATS = BM;
+    static constexpr int SB_FLOATS = BN;
+    static constexpr int SLOT_FLOATS = SA_FLOATS + SB_FLOATS;
+    static constexpr int COLS = BN / 2;                           // columns per epilogue warp
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SCALE = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_SCALE + SSLOTS * SLOT_FLOATS * 4;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 2 * SSLOTS;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment for 128-byte swizzle");
+    static_assert(COLS == 128, "epilogue chunking assumes 128 columns per warp");
+    // barrier indices
+    static __device__ __forceinline__ uint32_t full(int s) { return s; }
+    static __device__ __forceinline__ uint32_t empty(int s) { return STAGES + s; }
+    static __device__ __forceinline__ uint32_t tfull(int b) { return 2 * STAGES + b; }
+    static __device__ __forceinline__ uint32_t tempty(int b) { return 2 * STAGES + NBUF + b; }
+    static __device__ __forceinline__ uint32_t sfull(int i) { return 2 * STAGES + 2 * NBUF + i; }
+    static __device__ __forceinline__ uint32_t sempty(int i) { return 2 * STAGES + 2 * NBUF + SSLOTS + i; }
+};
+
 struct Params {
     int32_t m_tiles, n_tiles, kblocks;
     int32_t nb_valid;             // number of 128-column blocks of the output (cols / 128)
-    int64_t cols;                 // output row length
-    const float* sb;              // SB_SCALAR: scalar B-scale table
-    int64_t sb_stride_j;          // ... index = jb * sb_stride_j + b * sb_stride_b
-    int64_t sb_stride_b;
+    int64_t rows, cols;           // output shape
+    const float* sa;              // row scales, [kblocks][rows]
+    const float* sb;              // SB_SCALAR: scalar table, index jb * sb_stride_j + b * sb_stride_b
+    int64_t sb_stride_j;          //   (jb = 128-column block of the output, b = K block)
+    int64_t sb_stride_b;          // SB_VECTOR: column scales [kblocks][cols]
     uint16_t* out;                // BF16 [rows][cols]
     uint32_t* status;
     uint64_t timeout_ns;
     int32_t fault;                // test hook: withhold CTA 0's first operand copy
 };
-
-__device__ __forceinline__ uint32_t bar_full(int s) { return s; }
-__device__ __forceinline__ uint32_t bar_empty(int s) { return STAGES + s; }
-__device__ __forceinline__ uint32_t bar_tfull(int b) { return 2 * STAGES + b; }
-__device__ __forceinline__ uint32_t bar_tempty(int b) { return 2 * STAGES + 2 + b; }
-__device__ __forceinline__ uint32_t bar_sfull(int i) { return 2 * STAGES + 4 + i; }
-__device__ __forceinline__ uint32_t bar_sempty(int i) { return 2 * STAGES + 4 + SSLOTS + i; }
 
 // Bounded wait used while tearing down after an abort: ignores the abort
 // flag, only the time limit ends it.
@@ -103,52 +119,100 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     }
 }
 
-// acc[base + i] = fma(P[i], sc, acc[base + i]) for one 32-column chunk.
-__device__ __forceinline__ void promote_scalar(float (&acc)[128], int base, const uint32_t (&r)[32], float sc) {
+// Orders the uses of `r` after a preceding tcgen05.wait::ld (asm volatile
+// statements keep their order, and the uses depend on this one's outputs).
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// 16-byte global -> shared copy in the generic proxy, completed through
+// cp.async.mbarrier.arrive.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// acc[base + i] = fma(P[i], sc, acc[base + i]) for one 32-column chunk, two
+// columns per packed FP32 FMA (each lane of the pair rounds like fmaf).
+template <int N>
+__device__ __forceinline__ void promote_scalar(float (&acc)[N], int base, const uint32_t (&r)[32], float sc) {
+    const float2 s2 = make_float2(sc, sc);
 #pragma unroll
-    for (int i = 0; i < 32; i++) acc[base + i] = fmaf(__uint_as_float(r[i]), sc, acc[base + i]);
+    for (int i = 0; i < 32; i += 2) {
+        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), s2,
+                                    make_float2(acc[base + i], acc[base + i + 1]));
+        acc[base + i] = d.x;
+        acc[base + i + 1] = d.y;
+    }
 }
 
 // Rank-1 block scale (weight gradient): the FP32 product sa * sb[j] is
 // rounded first, then fused into the accumulator, as for a scalar scale.
-__device__ __forceinline__ void promote_vector(float (&acc)[128], int base, const uint32_t (&r)[32], float sa,
+template <int N>
+__device__ __forceinline__ void promote_vector(float (&acc)[N], int base, const uint32_t (&r)[32], float sa,
                                                const float* sbv) {
+    const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
         const float4 s4 = *reinterpret_cast<const float4*>(sbv + base + i);
-        acc[base + i + 0] = fmaf(__uint_as_float(r[i + 0]), __fmul_rn(sa, s4.x), acc[base + i + 0]);
-        acc[base + i + 1] = fmaf(__uint_as_float(r[i + 1]), __fmul_rn(sa, s4.y), acc[base + i + 1]);
-        acc[base + i + 2] = fmaf(__uint_as_float(r[i + 2]), __fmul_rn(sa, s4.z), acc[base + i + 2]);
-        acc[base + i + 3] = fmaf(__uint_as_float(r[i + 3]), __fmul_rn(sa, s4.w), acc[base + i + 3]);
+        const float2 c0 = __fmul2_rn(sa2, make_float2(s4.x, s4.y));
+        const float2 c1 = __fmul2_rn(sa2, make_float2(s4.z, s4.w));
+        const float2 d0 = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c0,
+                                     make_float2(acc[base + i], acc[base + i + 1]));
+        const float2 d1 = __ffma2_rn(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), c1,
+                                     make_float2(acc[base + i + 2], acc[base + i + 3]));
+        acc[base + i] = d0.x;
+        acc[base + i + 1] = d0.y;
+        acc[base + i + 2] = d1.x;
+        acc[base + i + 3] = d1.y;
     }
 }
 
-template <int SBMODE>
+template <int SBMODE, int N>
+__device__ __forceinline__ void promote(float (&acc)[N], int base, const uint32_t (&r)[32], float sa, float sc,
+                                        const float* sbv) {
+    if constexpr (SBMODE == SB_SCALAR)
+        promote_scalar(acc, base, r, sc);
+    else
+        promote_vector(acc, base, r, sa, sbv);
+}
+
+template <int SBMODE, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                const Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    using T = Tile<BN>;
+    constexpr int STAGES = T::STAGES, NBUF = T::NBUF, COLS = T::COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar0 = sbase + OFF_BAR;
+    const uint32_t bar0 = sbase + T::OFF_BAR;
     auto bar = [&](uint32_t i) { return bar0 + 8u * i; };
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);  // [0] TMEM base, [1] abort flag
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + T::OFF_MISC);  // [0] TMEM base, [1] abort flag
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
-            mbar_init(bar(bar_full(s)), 1);
-            mbar_init(bar(bar_empty(s)), 1);
+            mbar_init(bar(T::full(s)), 1);
+            mbar_init(bar(T::empty(s)), 1);
         }
-        for (int b = 0; b < 2; b++) {
-            mbar_init(bar(bar_tfull(b)), 1);
-            mbar_init(bar(bar_tempty(b)), NUM_EPI_WARPS);
+        for (int b = 0; b < NBUF; b++) {
+            mbar_init(bar(T::tfull(b)), 1);
+            mbar_init(bar(T::tempty(b)), NUM_EPI_WARPS);
         }
         for (int i = 0; i < SSLOTS; i++) {
-            mbar_init(bar(bar_sfull(i)), 1);
-            mbar_init(bar(bar_sempty(i)), NUM_EPI_WARPS);
+            mbar_init(bar(T::sfull(i)), 32);   // one cp.async arrival per lane of the scale warp
+            mbar_init(bar(T::sempty(i)), NUM_EPI_WARPS);
         }
         misc[1] = 0u;
         fence_mbar_init();
@@ -156,8 +220,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmSA);
-        if (SBMODE == SB_VECTOR) tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&misc[0]), TMEM_COLS);
@@ -177,22 +239,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int stage = 0, slot = 0;
-            uint32_t ph = 0, sph = 0;
+            int stage = 0;
+            uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0, inj = 0;      // per stage
-            uint32_t sarmed = 0, sarmed_par = 0;             // per scale slot
             bool ok = true;
-            constexpr uint32_t kScaleBytes = (SA_FLOATS + (SBMODE == SB_VECTOR ? SB_FLOATS : 0)) * 4;
             for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
                 const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
                 for (int kb = 0; kb < kblocks; kb++) {
-                    if (!wait_bounded(bar(bar_empty(stage)), ph ^ 1u, wc)) { ok = false; break; }
-                    const uint32_t fb = bar(bar_full(stage));
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    if (!wait_bounded(bar(T::empty(stage)), ph ^ 1u, wc)) { ok = false; break; }
+                    const uint32_t fb = bar(T::full(stage));
+                    mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
                     const bool inject = p.fault != 0 && blockIdx.x == 0 && t == static_cast<int>(blockIdx.x) && kb == 0;
                     if (!inject) {
-                        tma_load_2d(sbase + OFF_A + stage * A_BYTES, &tmA, kb * BK, mb * BM, fb);
-                        tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tmB, kb * BK, nb * BN, fb);
+                        tma_load_2d(sbase + T::OFF_A + stage * T::A_BYTES, &tmA, kb * BK, mb * BM, fb);
+                        tma_load_2d(sbase + T::OFF_B + stage * T::B_BYTES, &tmB, kb * BK, nb * BN, fb);
                         inj &= ~(1u << stage);
                     } else {
                         inj |= 1u << stage;
@@ -200,25 +260,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (ph << stage);
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
-
-                    if (!wait_bounded(bar(bar_sempty(slot)), sph ^ 1u, wc)) { ok = false; break; }
-                    const uint32_t sfb = bar(bar_sfull(slot));
-                    const uint32_t sdst = sbase + OFF_SCALE + slot * SLOT_FLOATS * 4;
-                    mbar_arrive_expect_tx(sfb, kScaleBytes);
-                    tma_load_2d(sdst, &tmSA, mb * BM, kb, sfb);
-                    if (SBMODE == SB_VECTOR) tma_load_2d(sdst + SA_FLOATS * 4, &tmSB, nb * BN, kb, sfb);
-                    sarmed |= 1u << slot;
-                    sarmed_par = (sarmed_par & ~(1u << slot)) | (sph << slot);
-                    if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
                 }
             }
             if (!ok) {
                 // Let every copy this CTA issued land before it exits.
                 for (int s = 0; s < STAGES; s++)
                     if (((armed >> s) & 1u) && !((inj >> s) & 1u))
-                        drain_wait(bar(bar_full(s)), (armed_par >> s) & 1u, p.timeout_ns);
-                for (int i = 0; i < SSLOTS; i++)
-                    if ((sarmed >> i) & 1u) drain_wait(bar(bar_sfull(i)), (sarmed_par >> i) & 1u, p.timeout_ns);
+                        drain_wait(bar(T::full(s)), (armed_par >> s) & 1u, p.timeout_ns);
             }
         }
       } else if (warp == 1) {
@@ -232,109 +280,127 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t last_tph = 0;
             for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
                 for (int kb = 0; kb < kblocks; kb++) {
-                    if (!wait_bounded(bar(bar_tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
+                    if (!wait_bounded(bar(T::tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
                     tc_fence_after();
-                    if (!wait_bounded(bar(bar_full(stage)), ph, wc)) { ok = false; break; }
+                    if (!wait_bounded(bar(T::full(stage)), ph, wc)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a0 = sbase + OFF_A + stage * A_BYTES;
-                    const uint32_t b0 = sbase + OFF_B + stage * B_BYTES;
+                    const uint32_t a0 = sbase + T::OFF_A + stage * T::A_BYTES;
+                    const uint32_t b0 = sbase + T::OFF_B + stage * T::B_BYTES;
                     const uint32_t d = tmem + static_cast<uint32_t>(tb * BN);
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; kk++)
                         mma_f8(d, sdesc_k_major_sw128(a0 + kk * 32), sdesc_k_major_sw128(b0 + kk * 32), idesc,
                                kk > 0 ? 1u : 0u);
-                    mma_commit(bar(bar_empty(stage)));
-                    mma_commit(bar(bar_tfull(tb)));
+                    mma_commit(bar(T::empty(stage)));
+                    mma_commit(bar(T::tfull(tb)));
                     issued = true;
                     last_tb = tb;
                     last_tph = tph;
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
-                    tb ^= 1;
-                    if (tb == 0) tph ^= 1u;
+                    if (++tb == NBUF) { tb = 0; tph ^= 1u; }
                 }
             }
-            if (!ok && issued) drain_wait(bar(bar_tfull(last_tb)), last_tph, p.timeout_ns);
+            if (!ok && issued) drain_wait(bar(T::tfull(last_tb)), last_tph, p.timeout_ns);
         }
+      } else if (warp == 2) {
+        // ------------------------------------------------ scale loader
+        int slot = 0;
+        uint32_t sph = 0;
+        bool ok = true;
+        const uint32_t ring = sbase + T::OFF_SCALE;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
+            for (int kb = 0; kb < kblocks; kb++) {
+                if (!warp_wait_bounded(bar(T::sempty(slot)), sph ^ 1u, wc)) { ok = false; break; }
+                const uint32_t dst = ring + static_cast<uint32_t>(slot * T::SLOT_FLOATS * 4);
+                cp_async_16(dst + lane * 16, p.sa + static_cast<int64_t>(kb) * p.rows + mb * BM + lane * 4);
+                if constexpr (SBMODE == SB_VECTOR) {
+#pragma unroll
+                    for (int c = 0; c < BN / 128; c++) {
+                        // Columns past the output's end (a ragged last tile) copy any valid
+                        // scale: those columns are computed but never stored.
+                        int64_t col = static_cast<int64_t>(nb) * BN + c * 128 + lane * 4;
+                        if (col >= p.cols) col = 0;
+                        cp_async_16(dst + (T::SA_FLOATS + c * 128) * 4 + lane * 16,
+                                    p.sb + static_cast<int64_t>(kb) * p.cols + col);
+                    }
+                }
+                cp_async_arrive(bar(T::sfull(slot)));
+                if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
+            }
+        }
+        cp_async_wait_all();
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
         // ------------------------------------------------ promotion + epilogue
         const int ew = warp - 4;
         const int quad = warp & 3;   // TMEM lanes this warp may access
-        const int half = ew >> 2;    // 128-column half of the tile
+        const int half = ew >> 2;    // column half of the tile
         const int row = quad * 32 + lane;
-        const float* ring = reinterpret_cast<const float*>(smem + OFF_SCALE);
+        const float* ring = reinterpret_cast<const float*>(smem + T::OFF_SCALE);
         int tb = 0, slot = 0;
         uint32_t tph = 0, sph = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
-            const int jb = nb * 2 + half;
+            // 128-column block of the output this warp's columns fall in
+            const int jb = (nb * BN + half * COLS) >> 7;
             const bool jvalid = jb < p.nb_valid;
-            float acc[128];
+            float acc[COLS];
 #pragma unroll
-            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
+            for (int i = 0; i < COLS; i++) acc[i] = 0.0f;
             float sb_next = 0.0f;
             if (SBMODE == SB_SCALAR && jvalid) sb_next = __ldg(p.sb + jb * p.sb_stride_j);
             for (int kb = 0; kb < kblocks; kb++) {
                 const float sb_cur = sb_next;
                 if (SBMODE == SB_SCALAR && jvalid && kb + 1 < kblocks)
                     sb_next = __ldg(p.sb + jb * p.sb_stride_j + (kb + 1) * p.sb_stride_b);
-                if (!warp_wait_bounded(bar(bar_sfull(slot)), sph, wc)) { ok = false; break; }
-                const float* sl = ring + slot * SLOT_FLOATS;
+                if (!warp_wait_bounded(bar(T::sfull(slot)), sph, wc)) { ok = false; break; }
+                const float* sl = ring + slot * T::SLOT_FLOATS;
                 const float sa = sl[row];
-                if (!warp_wait_bounded(bar(bar_tfull(tb)), tph, wc)) { ok = false; break; }
+                const float sc = __fmul_rn(sa, sb_cur);
+                const float* sbv = sl + T::SA_FLOATS + half * COLS;
+                if constexpr (SBMODE == SB_SCALAR) {
+                    // Only the row scale is needed from the slot: free it now.
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::sempty(slot)));
+                }
+                if (!warp_wait_bounded(bar(T::tfull(tb)), tph, wc)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       static_cast<uint32_t>(tb * BN + half * 128);
-                // Chunk c+1's TMEM load is in flight while chunk c is promoted.
+                                       static_cast<uint32_t>(tb * BN + half * COLS);
+                // Two 32-column chunks in flight per wait; the TMEM buffer is
+                // released as soon as the last chunk is in registers.
                 uint32_t ra[32], rb[32];
-                if (SBMODE == SB_SCALAR) {
-                    const float sc = __fmul_rn(sa, sb_cur);
-                    tmem_ld_32cols(taddr + 0, ra);
-                    tmem_wait_ld(ra);
-                    tmem_ld_32cols(taddr + 32, rb);
-                    promote_scalar(acc, 0, ra, sc);
-                    tmem_wait_ld(rb);
-                    tmem_ld_32cols(taddr + 64, ra);
-                    promote_scalar(acc, 32, rb, sc);
-                    tmem_wait_ld(ra);
-                    tmem_ld_32cols(taddr + 96, rb);
-                    promote_scalar(acc, 64, ra, sc);
-                    tmem_wait_ld(rb);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(bar_tempty(tb)));
-                    promote_scalar(acc, 96, rb, sc);
-                } else {
-                    const float* sbv = sl + SA_FLOATS + half * 128;
-                    tmem_ld_32cols(taddr + 0, ra);
-                    tmem_wait_ld(ra);
-                    tmem_ld_32cols(taddr + 32, rb);
-                    promote_vector(acc, 0, ra, sa, sbv);
-                    tmem_wait_ld(rb);
-                    tmem_ld_32cols(taddr + 64, ra);
-                    promote_vector(acc, 32, rb, sa, sbv);
-                    tmem_wait_ld(ra);
-                    tmem_ld_32cols(taddr + 96, rb);
-                    promote_vector(acc, 64, ra, sa, sbv);
-                    tmem_wait_ld(rb);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(bar_tempty(tb)));
-                    promote_vector(acc, 96, rb, sa, sbv);
-                }
+                tmem_ld_32cols(taddr + 0, ra);
+                tmem_ld_32cols(taddr + 32, rb);
+                tmem_wait_ld(ra);
+                reg_fence(rb);
+                promote<SBMODE>(acc, 0, ra, sa, sc, sbv);
+                promote<SBMODE>(acc, 32, rb, sa, sc, sbv);
+                tmem_ld_32cols(taddr + 64, ra);
+                tmem_ld_32cols(taddr + 96, rb);
+                tmem_wait_ld(ra);
+                reg_fence(rb);
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bar_sempty(slot)));
-                tb ^= 1;
-                if (tb == 0) tph ^= 1u;
+                if (lane == 0) mbar_arrive(bar(T::tempty(tb)));
+                promote<SBMODE>(acc, 64, ra, sa, sc, sbv);
+                promote<SBMODE>(acc, 96, rb, sa, sc, sbv);
+                if constexpr (SBMODE == SB_VECTOR) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::sempty(slot)));
+                }
+                if (++tb == NBUF) { tb = 0; tph ^= 1u; }
                 if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
             }
             if (!ok) break;
             if (jvalid) {
-                uint16_t* orow = p.out + (static_cast<int64_t>(mb) * BM + row) * p.cols + static_cast<int64_t>(jb) * 128;
+                uint16_t* orow = p.out + (static_cast<int64_t>(mb) * BM + row) * p.cols +
+                                 static_cast<int64_t>(nb) * BN + half * COLS;
 #pragma unroll
-                for (int j = 0; j < 128; j += 8) {
+                for (int j = 0; j < COLS; j += 8) {
                     uint4 v;
                     v.x = f32x2_to_bf16x2(acc[j + 0], acc[j + 1]);
                     v.y = f32x2_to_bf16x2(acc[j + 2], acc[j + 3]);
