@@ -236,54 +236,58 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
+      // The producer and MMA warps run their loops with all 32 lanes
+      // converged (waits are warp-wide); only lane 0 issues the TMA and
+      // tcgen05 instructions.  A lone lane looping while its warp-mates
+      // park at the final barrier slows the other warps of its SM
+      // sub-partition.
       if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t ph = 0;
-            uint32_t armed = 0, armed_par = 0, inj = 0;      // per stage
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
-                for (int kb = 0; kb < kblocks; kb++) {
-                    if (!wait_bounded(bar(T::empty(stage)), ph ^ 1u, wc)) { ok = false; break; }
+        int stage = 0;
+        uint32_t ph = 0;
+        uint32_t armed = 0, armed_par = 0, inj = 0;      // per stage
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
+            for (int kb = 0; kb < kblocks; kb++) {
+                if (!warp_wait_bounded(bar(T::empty(stage)), ph ^ 1u, wc)) { ok = false; break; }
+                const bool inject = p.fault != 0 && blockIdx.x == 0 && t == static_cast<int>(blockIdx.x) && kb == 0;
+                if (lane == 0) {
                     const uint32_t fb = bar(T::full(stage));
                     mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
-                    const bool inject = p.fault != 0 && blockIdx.x == 0 && t == static_cast<int>(blockIdx.x) && kb == 0;
                     if (!inject) {
                         tma_load_2d(sbase + T::OFF_A + stage * T::A_BYTES, &tmA, kb * BK, mb * BM, fb);
                         tma_load_2d(sbase + T::OFF_B + stage * T::B_BYTES, &tmB, kb * BK, nb * BN, fb);
-                        inj &= ~(1u << stage);
-                    } else {
-                        inj |= 1u << stage;
                     }
-                    armed |= 1u << stage;
-                    armed_par = (armed_par & ~(1u << stage)) | (ph << stage);
-                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 }
-            }
-            if (!ok) {
-                // Let every copy this CTA issued land before it exits.
-                for (int s = 0; s < STAGES; s++)
-                    if (((armed >> s) & 1u) && !((inj >> s) & 1u))
-                        drain_wait(bar(T::full(s)), (armed_par >> s) & 1u, p.timeout_ns);
+                __syncwarp();
+                if (!inject) inj &= ~(1u << stage); else inj |= 1u << stage;
+                armed |= 1u << stage;
+                armed_par = (armed_par & ~(1u << stage)) | (ph << stage);
+                if (++stage == STAGES) { stage = 0; ph ^= 1u; }
             }
         }
+        if (!ok && lane == 0) {
+            // Let every copy this CTA issued land before it exits.
+            for (int s = 0; s < STAGES; s++)
+                if (((armed >> s) & 1u) && !((inj >> s) & 1u))
+                    drain_wait(bar(T::full(s)), (armed_par >> s) & 1u, p.timeout_ns);
+        }
+        __syncwarp();
       } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-            int stage = 0, tb = 0;
-            uint32_t ph = 0, tph = 0;
-            bool ok = true, issued = false;
-            int last_tb = 0;
-            uint32_t last_tph = 0;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                for (int kb = 0; kb < kblocks; kb++) {
-                    if (!wait_bounded(bar(T::tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    if (!wait_bounded(bar(T::full(stage)), ph, wc)) { ok = false; break; }
-                    tc_fence_after();
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+        int stage = 0, tb = 0;
+        uint32_t ph = 0, tph = 0;
+        bool ok = true, issued = false;
+        int last_tb = 0;
+        uint32_t last_tph = 0;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            for (int kb = 0; kb < kblocks; kb++) {
+                if (!warp_wait_bounded(bar(T::tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
+                if (!warp_wait_bounded(bar(T::full(stage)), ph, wc)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
                     const uint32_t a0 = sbase + T::OFF_A + stage * T::A_BYTES;
                     const uint32_t b0 = sbase + T::OFF_B + stage * T::B_BYTES;
                     const uint32_t d = tmem + static_cast<uint32_t>(tb * BN);
@@ -293,15 +297,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                                kk > 0 ? 1u : 0u);
                     mma_commit(bar(T::empty(stage)));
                     mma_commit(bar(T::tfull(tb)));
-                    issued = true;
-                    last_tb = tb;
-                    last_tph = tph;
-                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
-                    if (++tb == NBUF) { tb = 0; tph ^= 1u; }
                 }
+                __syncwarp();
+                issued = true;
+                last_tb = tb;
+                last_tph = tph;
+                if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                if (++tb == NBUF) { tb = 0; tph ^= 1u; }
             }
-            if (!ok && issued) drain_wait(bar(T::tfull(last_tb)), last_tph, p.timeout_ns);
         }
+        if (!ok && issued && lane == 0) drain_wait(bar(T::tfull(last_tb)), last_tph, p.timeout_ns);
+        __syncwarp();
       } else if (warp == 2) {
         // ------------------------------------------------ scale loader
         int slot = 0;

@@ -53,6 +53,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet is
+// suspended in hardware until the phase completes or about `hint_ns`
+// nanoseconds pass, instead of returning at once; waiting threads then
+// issue no polling traffic.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspension granted per try in the bounded waits below; the abort flag and
+// the time limit are checked between tries.
+constexpr uint32_t kWaitSliceNs = 20000;
+
 // Shared state every bounded wait of one CTA consults.
 struct WaitCtx {
     volatile uint32_t* abort_flag;  // shared memory: set once any role gives up
@@ -67,7 +87,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSliceNs)) return true;
         if (*w.abort_flag) return false;
         if (global_timer_ns() - t0 > w.timeout_ns) {
             *w.abort_flag = 1u;
