@@ -2,11 +2,12 @@
 // shapes of the fine-grained block quantization (1x128 activation tiles,
 // 128x1 token-dim tiles written transposed, 128x128 weight blocks).
 //
-// One CTA owns one 128x128 BF16 tile of the input (32 KB): it stages the
-// tile in shared memory with 16-byte coalesced loads, then computes
+// One CTA owns one 128x128 BF16 tile of the input (32 KB): it copies the
+// tile into shared memory with 16-byte cp.async copies (no staging
+// registers, so five CTAs fit on an SM and their load, compute and store
+// phases overlap), then computes
 //   - row maxima (1x128 tiles) with a bank-skewed row sweep,
-//   - column maxima (128x1 tiles, or the 128x128 block) with a column sweep
-//     whose 32 words per thread stay in registers for the transposed cast,
+//   - column maxima (128x1 tiles, or the 128x128 block) with a column sweep,
 // on the BF16 bit patterns (|x| ordering equals the ordering of the
 // sign-cleared bits, so a packed 16-bit unsigned max is exact), then one
 // IEEE division pair per tile for s = amax/448 and inv = 448/amax, then
@@ -38,12 +39,18 @@ __device__ __forceinline__ void tile_scale(float amax, float& s, float& inv) {
     inv = fminf(__fdiv_rn(448.0f, amax), FLT_MAX);
 }
 
-__device__ __forceinline__ uint32_t e4m3x4_lo(uint32_t w0, uint32_t w1, float iv) {
-    // low BF16 halves of two words: elements (w0.lo, w1.lo)
-    return e4m3x2(__fmul_rn(bf16lo_to_f32(w0), iv), __fmul_rn(bf16lo_to_f32(w1), iv));
+// Four E4M3 codes from the low (lo = true) or high BF16 halves of four words.
+__device__ __forceinline__ uint32_t e4m3x4_half(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, float iv,
+                                                bool lo) {
+    const float a = lo ? bf16lo_to_f32(w0) : bf16hi_to_f32(w0);
+    const float b = lo ? bf16lo_to_f32(w1) : bf16hi_to_f32(w1);
+    const float c = lo ? bf16lo_to_f32(w2) : bf16hi_to_f32(w2);
+    const float d = lo ? bf16lo_to_f32(w3) : bf16hi_to_f32(w3);
+    return e4m3x2(__fmul_rn(a, iv), __fmul_rn(b, iv)) | (e4m3x2(__fmul_rn(c, iv), __fmul_rn(d, iv)) << 16);
 }
-__device__ __forceinline__ uint32_t e4m3x4_hi(uint32_t w0, uint32_t w1, float iv) {
-    return e4m3x2(__fmul_rn(bf16hi_to_f32(w0), iv), __fmul_rn(bf16hi_to_f32(w1), iv));
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 // x: BF16 [rows][cols] viewed as 32-bit words (two BF16 per word).
@@ -52,10 +59,10 @@ __device__ __forceinline__ uint32_t e4m3x4_hi(uint32_t w0, uint32_t w1, float iv
 // MODE == QM_BLOCK: q [rows][cols], qT [cols][rows] (nullable),
 //                   s [rows/128][cols/128]
 template <int MODE>
-__global__ void __launch_bounds__(256) quant_tile_kernel(const uint32_t* __restrict__ x, int64_t rows,
-                                                         int64_t cols, uint8_t* __restrict__ q,
-                                                         float* __restrict__ s, uint8_t* __restrict__ qT,
-                                                         float* __restrict__ sT) {
+__global__ void __launch_bounds__(256, 5) quant_tile_kernel(const uint32_t* __restrict__ x, int64_t rows,
+                                                            int64_t cols, uint8_t* __restrict__ q,
+                                                            float* __restrict__ s, uint8_t* __restrict__ qT,
+                                                            float* __restrict__ sT) {
     constexpr bool kRow = (MODE & QM_ROW) != 0;
     constexpr bool kColT = (MODE & QM_COLT) != 0;
     constexpr bool kBlock = (MODE & QM_BLOCK) != 0;
@@ -74,34 +81,26 @@ __global__ void __launch_bounds__(256) quant_tile_kernel(const uint32_t* __restr
     const int64_t wpr = cols >> 1;  // words per row
 
     // 1. The 128x128 tile into shared memory: 2048 chunks of 16 bytes, eight
-    //    per thread, all loads issued before the first use.
+    //    per thread, all in flight at once.
     {
         const uint32_t* src = x + r0 * wpr + (c0 >> 1);
-        uint4 v[8];
+        const uint32_t dst = smem_u32(tile);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             const int id = i * 256 + tid, r = id >> 4, ch = id & 15;
-            v[i] = ld_nc_v4(src + r * wpr + ch * 4);
+            cp_async16(dst + static_cast<uint32_t>(r * 256 + ch * 16), src + r * wpr + ch * 4);
         }
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const int id = i * 256 + tid, r = id >> 4, ch = id & 15;
-            *reinterpret_cast<uint4*>(&tile[r * 64 + ch * 4]) = v[i];
-        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     __syncthreads();
 
     // 2a. Column sweep: thread -> column pair cp (columns 2cp, 2cp+1), rows
     //     [32 seg, 32 seg + 32).  Lanes read consecutive words: no conflicts.
     const int cp = tid & 63, seg = tid >> 6;
-    uint32_t cw[kNeedCol ? 32 : 1];
     if constexpr (kNeedCol) {
         uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-            cw[i] = tile[(seg * 32 + i) * 64 + cp];
-            m = max_u16x2(m, cw[i] & 0x7FFF7FFFu);
-        }
+#pragma unroll 8
+        for (int i = 0; i < 32; i++) m = max_u16x2(m, tile[(seg * 32 + i) * 64 + cp] & 0x7FFF7FFFu);
         cpart[seg][cp] = m;
     }
     // 2b. Row sweep: thread -> row tid/2, half tid%2; word order skewed by
@@ -109,7 +108,7 @@ __global__ void __launch_bounds__(256) quant_tile_kernel(const uint32_t* __restr
     if constexpr (kRow) {
         const int r = tid >> 1, h = tid & 1;
         uint32_t m = 0;
-#pragma unroll
+#pragma unroll 8
         for (int j = 0; j < 32; j++) m = max_u16x2(m, tile[r * 64 + h * 32 + ((j + lane) & 31)] & 0x7FFF7FFFu);
         m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
         if (h == 0) rmax[r] = max(m & 0xFFFFu, m >> 16);
@@ -168,24 +167,47 @@ __global__ void __launch_bounds__(256) quant_tile_kernel(const uint32_t* __restr
         }
     }
 
-    // 4b. Transposed payload: thread (cp, seg) writes 32 bytes of qT rows
-    //     2cp and 2cp+1 (tokens [32 seg, 32 seg + 32) of this tile).
+    // 4b. Transposed payload: thread (cp, seg) converts 32 tokens of columns
+    //     2cp and 2cp+1 (re-reading the column words from shared memory),
+    //     then, once every read of the tile is done, parks its 2 x 32 bytes
+    //     in the tile buffer as rows of a [128 columns][128 tokens] byte
+    //     block (row stride 144 bytes, which spreads both the parking writes
+    //     and the reads below over all banks), and the CTA writes that block
+    //     out as full 128-byte lines of qT.
     if constexpr (kNeedCol) {
         if (kColT || qT != nullptr) {
             const float ivl = kColT ? cinv[2 * cp] : binv;
             const float ivh = kColT ? cinv[2 * cp + 1] : binv;
-            uint32_t pl[8], ph[8];
+            uint4 pl[2], ph[2];
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                pl[i] = e4m3x4_lo(cw[4 * i], cw[4 * i + 1], ivl) | (e4m3x4_lo(cw[4 * i + 2], cw[4 * i + 3], ivl) << 16);
-                ph[i] = e4m3x4_hi(cw[4 * i], cw[4 * i + 1], ivh) | (e4m3x4_hi(cw[4 * i + 2], cw[4 * i + 3], ivh) << 16);
+            for (int g = 0; g < 2; g++) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) w[i] = tile[(seg * 32 + g * 16 + i) * 64 + cp];
+                pl[g].x = e4m3x4_half(w[0], w[1], w[2], w[3], ivl, true);
+                pl[g].y = e4m3x4_half(w[4], w[5], w[6], w[7], ivl, true);
+                pl[g].z = e4m3x4_half(w[8], w[9], w[10], w[11], ivl, true);
+                pl[g].w = e4m3x4_half(w[12], w[13], w[14], w[15], ivl, true);
+                ph[g].x = e4m3x4_half(w[0], w[1], w[2], w[3], ivh, false);
+                ph[g].y = e4m3x4_half(w[4], w[5], w[6], w[7], ivh, false);
+                ph[g].z = e4m3x4_half(w[8], w[9], w[10], w[11], ivh, false);
+                ph[g].w = e4m3x4_half(w[12], w[13], w[14], w[15], ivh, false);
             }
-            uint8_t* dl = qT + (c0 + 2 * cp) * rows + r0 + seg * 32;
-            uint8_t* dh = dl + rows;
-            reinterpret_cast<uint4*>(dl)[0] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-            reinterpret_cast<uint4*>(dl)[1] = make_uint4(pl[4], pl[5], pl[6], pl[7]);
-            reinterpret_cast<uint4*>(dh)[0] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-            reinterpret_cast<uint4*>(dh)[1] = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+            constexpr int kStride = 144;  // bytes per parked qT row
+            uint8_t* park = reinterpret_cast<uint8_t*>(tile);
+            __syncthreads();  // every read of the BF16 tile is done
+#pragma unroll
+            for (int g = 0; g < 2; g++) {
+                *reinterpret_cast<uint4*>(park + (2 * cp) * kStride + seg * 32 + g * 16) = pl[g];
+                *reinterpret_cast<uint4*>(park + (2 * cp + 1) * kStride + seg * 32 + g * 16) = ph[g];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int id = i * 256 + tid, rr = id >> 3, part = id & 7;
+                const uint4 v = *reinterpret_cast<const uint4*>(park + rr * kStride + part * 16);
+                *reinterpret_cast<uint4*>(qT + (c0 + rr) * rows + r0 + part * 16) = v;
+            }
         }
     }
 }
