@@ -59,7 +59,7 @@ def load_peaks():
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons every 20 ms while running."""
+    """Samples SM clock and clock-event reasons every 5 ms while running."""
 
     REASONS = {
         "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
@@ -105,7 +105,7 @@ class ClockSampler:
                     self.samples.append((a, 0))
             except Exception:
                 pass
-            self._stop.wait(0.02)
+            self._stop.wait(0.005)
 
     def stop(self):
         self._stop.set()
@@ -147,22 +147,6 @@ def time_step(launch_lists, steps, per_launch):
     torch.cuda.synchronize()
     per = [(l, a.elapsed_time(b)) for l, a, b in marks]
     return t0.elapsed_time(t1), per
-
-
-def summarize(per):
-    agg = {}
-    for l, ms in per:
-        a = agg.setdefault(l.op, {"launches": 0, "ms": 0.0, "work": 0, "unit": l.unit})
-        a["launches"] += 1
-        a["ms"] += ms
-        a["work"] += l.work
-    return agg
-
-
-def op_rate(a):
-    if a["unit"] == "flops":
-        return a["work"] / (a["ms"] * 1e-3) / 1e12, "TFLOP/s"
-    return a["work"] / (a["ms"] * 1e-3) / 1e9, "GB/s"
 
 
 def flush_l2(buf):
@@ -246,37 +230,97 @@ def e2e_run(wl, steps_data, steps):
     return dt, h2d, d2h
 
 
-def cpu_sample(lin_data, rows):
-    """The oracle (single-threaded C) on a bounded sample of the step: for
-    each linear, the first 128 tokens quantized both ways and W quantized in
-    full, then `rows` rows of fprop and dgrad and `rows` rows of wgrad over
-    that token block.  Returns (flops, seconds)."""
+def cpu_sample(lin_data, feats, rows, tokens=128):
+    """The oracle (single-threaded C) on a bounded sample of the step: each
+    linear restricted to its first `tokens` tokens and first `feats` output
+    features (all input features), i.e. X[:tokens], W[:feats],
+    dY[:tokens, :feats], run through every step of the path -- both
+    quantizations of X and dY, the 128x128 weight quantization, then `rows`
+    output rows of fprop, dgrad and wgrad of that sub-problem.  Returns
+    (GEMM flops of the sampled rows, seconds), so that flops/seconds is in
+    the same unit as the GPU figure (GEMM work over the whole path's time)."""
     import numpy as np
 
     import oracle
 
     flops, t = 0, time.perf_counter()
     for lin, d in lin_data:
-        x = d["x"][:128].cpu()
-        w = d["w"].cpu()
-        N, K = w.shape
-        r = np.arange(rows)
+        K = lin.in_features
+        F = min(feats, lin.out_features)
+        x = d["x"][:tokens].cpu().contiguous()
+        w = d["w"][:F].cpu().contiguous()
+        r = np.arange(min(rows, tokens))
         xq, sx = oracle.quant_rowwise_1x128(x)
         wq, _, sw = oracle.quant_weight_128x128(w, want_t=False)
         oracle.gemm_fprop(xq, sx, wq, sw, rows=r)
-        flops += 2 * rows * N * K
+        flops += 2 * r.size * F * K
+        if "dgrad" in lin.ops or "wgrad" in lin.ops:
+            dy = d["dy"][:tokens, :F].cpu().contiguous()
         if "dgrad" in lin.ops:
-            dy = d["dy"][:128].cpu()
             dyq, sdy = oracle.quant_rowwise_1x128(dy)
             oracle.gemm_dgrad(dyq, sdy, wq, sw, rows=r)
-            flops += 2 * rows * N * K
+            flops += 2 * r.size * K * F
         if "wgrad" in lin.ops:
-            dy = d["dy"][:128].cpu()
             xTq, sxT = oracle.quant_colwise_128x1_T(x)
             dyTq, sdyT = oracle.quant_colwise_128x1_T(dy)
-            oracle.gemm_wgrad(dyTq, sdyT, xTq, sxT, rows=r)
-            flops += 2 * rows * K * 128
+            rw = np.arange(min(rows, F))
+            oracle.gemm_wgrad(dyTq, sdyT, xTq, sxT, rows=rw)
+            flops += 2 * rw.size * K * tokens
     return flops, time.perf_counter() - t
+
+
+def sample_note(feats, rows, tokens=128):
+    return (f"each linear restricted to its first {tokens} tokens and first {feats} output features (all input "
+            f"features): X and dY quantized both ways, W[:{feats}] quantized 128x128, {rows} output rows of "
+            f"fprop, dgrad and wgrad; single-threaded C oracle")
+
+
+KERNEL_OF_OP = {
+    "fprop": "gemm_kernel<SB_SCALAR>", "dgrad": "gemm_kernel<SB_SCALAR>", "wgrad": "gemm_kernel<SB_VECTOR>",
+    "quant_act": "quant_tile_kernel<QM_ROW|QM_COLT>", "quant_weight": "quant_tile_kernel<QM_BLOCK>",
+}
+
+
+def summarize_kernels(per):
+    """Per kernel function: launches, summed event time, algorithmic work."""
+    agg = {}
+    for l, ms in per:
+        k = KERNEL_OF_OP[l.op]
+        a = agg.setdefault(k, {"launches": 0, "ms": 0.0, "work": 0, "unit": l.unit, "ops": set()})
+        a["launches"] += 1
+        a["ms"] += ms
+        a["work"] += l.work
+        a["ops"].add(l.op)
+    return agg
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources; a stored ncu traffic figure is only used
+    while the kernels it was measured on are unchanged."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_block_scaled_16_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None if absent or stale."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t["kernels"][kernel]
+        if t.get("source_hash") != kernel_source_hash() or t.get("workload") != workload:
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
 
 
 def run_ours(args):
@@ -321,27 +365,39 @@ def run_ours(args):
     ms_max = D.max_over_ranks(ranks, ms_step, device)
     value = flops_step * ranks.world / (ms_max * 1e-3) / 1e12
 
-    agg = summarize(per)
-    dom_op = max(agg, key=lambda k: agg[k]["ms"])
-    a = agg[dom_op]
-    rate, runit = op_rate(a)
+    # Roofline of the kernel with the largest share of the step: algorithmic
+    # work of its launches / their summed event time, over the timed region.
+    agg = summarize_kernels(per)
+    dom = max(agg, key=lambda k: agg[k]["ms"])
+    a = agg[dom]
+    per_launch_ms = a["ms"] / a["launches"]
     long_region = total_ms >= 2000.0
+    traffic = stored_traffic(dom, wl.name)
     if a["unit"] == "flops":
+        rate = a["work"] / (a["ms"] * 1e-3) / 1e12
         peak = fp8_sust if long_region else fp8_burst
-        roof = {"bound": "tensor", "kernel": dom_op, "achieved": round(rate, 1), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(rate / peak, 4), "traffic": None,
-                "peak_note": (f"FP8 = {'sustained' if long_region else 'burst'} bf16 cuBLAS "
-                              f"x {FP8_PER_BF16:g} (nominal FP8:BF16), {peak_src}")}
+        roof = {"bound": "tensor", "achieved": round(rate, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(rate / peak, 4), "traffic": traffic, "kernel": dom,
+                "ops": sorted(a["ops"]), "launches_per_step": a["launches"] // args.steps,
+                "avg_launch_ms": round(per_launch_ms, 4),
+                "peak_note": (f"dense FP8 = {'sustained' if long_region else 'burst'} cuBLAS bf16 of measured "
+                              f"x {FP8_PER_BF16:g} (nominal FP8:BF16 ratio); {peak_src}")}
     else:
-        roof = {"bound": "hbm", "kernel": dom_op, "achieved": round(rate, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(rate / peaks["hbm_gbs"], 4), "traffic": None,
-                "peak_note": f"STREAM-style copy, {peak_src}"}
+        rate = a["work"] / (a["ms"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(rate, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(rate / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": dom,
+                "ops": sorted(a["ops"]), "launches_per_step": a["launches"] // args.steps,
+                "avg_launch_ms": round(per_launch_ms, 4), "peak_note": f"STREAM-style copy, {peak_src}"}
     breakdown = {}
-    for op, s in sorted(agg.items()):
-        r, u = op_rate(s)
-        frac = r / (fp8_burst if u == "TFLOP/s" else peaks["hbm_gbs"])
-        breakdown[op] = {"launches": s["launches"] // args.steps, "ms_per_step": round(s["ms"] / args.steps, 4),
-                         u: round(r, 1), "frac": round(frac, 3)}
+    for k, s in sorted(agg.items(), key=lambda kv: -kv[1]["ms"]):
+        if s["unit"] == "flops":
+            r, u, pk = s["work"] / (s["ms"] * 1e-3) / 1e12, "TFLOP/s", fp8_burst
+        else:
+            r, u, pk = s["work"] / (s["ms"] * 1e-3) / 1e9, "GB/s", peaks["hbm_gbs"]
+        breakdown[k] = {"ops": sorted(s["ops"]), "launches_per_step": s["launches"] // args.steps,
+                        "ms_per_step": round(s["ms"] / args.steps, 4),
+                        "share": round(s["ms"] / sum(v["ms"] for v in agg.values()), 4),
+                        u: round(r, 1), "frac_of_measured": round(r / pk, 3)}
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ranks.world,
@@ -350,12 +406,13 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": wl.name, "tokens": wl.linears[0].tokens,
                    "linears": [f"{l.name} {l.in_features}->{l.out_features}" for l in wl.linears],
-                   "step": "quant X (1x128+128x1T), quant W (128x128+T), fprop, quant dY (1x128+128x1T), "
-                           "dgrad, wgrad per linear",
+                   "step": "per linear: quantize X (1x128 + 128x1 transposed, one read), quantize W (128x128 "
+                           "+ transposed copy), fprop, quantize dY (both layouts), dgrad, wgrad",
                    "gemm_tflop_per_step": round(flops_step / 1e12, 4),
-                   "l2": f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of BF16 inputs per step, L2 126 MB)",
-                   "inputs": "drawn on the GPU with torch's CUDA generator (recipe in inputs.py)",
-                   "parallelism": f"replicas x{ranks.world}" if ranks.world > 1 else "single GPU"},
+                   "l2": f"no flush: inputs larger than L2 ({in_bytes / 1e9:.2f} GB of BF16 inputs per step; "
+                         f"L2 126 MB)",
+                   "inputs": "drawn on the GPU with torch's CUDA generator (distributions as in inputs.py)",
+                   "parallelism": f"independent replicas x{ranks.world}" if ranks.world > 1 else "single GPU"},
         "roofline": roof, "breakdown": breakdown, "gpu_launches": launched,
         "gpu_launches_expected": launches_step * args.steps, "clocks": clk,
     }
@@ -366,16 +423,14 @@ def run_ours(args):
         dt_max = D.max_over_ranks(ranks, dt, device)
         result["e2e"] = {"value": round(flops_step * ranks.world / dt_max / 1e12, 2), "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "ms_per_step": round(dt_max * 1e3, 2),
-                         "note": "pinned host inputs copied in and results copied out every step, via the "
-                                 "Python binding of the C ABI"}
+                         "ms_per_step": round(dt_max * 1e3, 2), "steps": e2e_steps,
+                         "note": "every step copies X, W, dY in from pinned host memory and Y, dX, dW back out, "
+                                 "around the same library calls (host clock, stream synchronized per step)"}
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu:
-        rows = args.cpu_rows
-        fl, sec = cpu_sample(list(zip(wl.linears, data)), rows)
+        fl, sec = cpu_sample(list(zip(wl.linears, data)), args.cpu_feats, args.cpu_rows)
         result["cpu_baseline"] = {
             "value": fl / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first 128 tokens of each linear quantized both ways, W quantized in full, {rows} rows of "
-                      f"fprop, dgrad and wgrad per linear; single-threaded C oracle, {sec:.1f} s"}
+            "sample": sample_note(args.cpu_feats, args.cpu_rows) + f", {sec:.1f} s"}
     if ranks.world == 1 and not args.no_sweep:
         result["per_workload"] = sweep(peaks, fp8_burst)
     if ranks.rank == 0:
@@ -386,29 +441,39 @@ def run_ours(args):
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
-    ranks = D.Ranks(int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0, False)
-    if ranks.rank != 0:
+    """The oracle as it stands, on the host cores, on bounded samples of the
+    same workload (rank 0 only; other ranks exit without work)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
         return
     wl = inputs.WORKLOADS[args.workload]
-    data = inputs.make_linear_inputs(wl, device="cpu")
-    lin_data = list(zip(wl.linears, data))
-    rows = args.ref_rows
+    tokens = 128
+    data = []
+    for lin in wl.linears:
+        # The sample only touches the first 128 tokens: draw just those (same
+        # distributions as the workload's recipe, CPU generator).
+        sub = inputs.Workload(wl.name, wl.seed, (inputs.Linear(lin.name, tokens, lin.in_features,
+                                                               lin.out_features, lin.ops),),
+                              wl.x_dist, wl.outliers, wl.outlier_factor)
+        data.append((lin, inputs.make_linear_inputs(sub, device="cpu")[0]))
+    feats, rows = args.ref_feats, args.ref_rows
     for _ in range(args.warmup):
-        cpu_sample(lin_data, rows)
+        cpu_sample(data, feats, rows)
     fl = sec = 0.0
     for _ in range(args.steps):
-        f, s = cpu_sample(lin_data, rows)
+        f, s = cpu_sample(data, feats, rows)
         fl += f
         sec += s
     value = fl / sec / 1e12
-    sample = (f"first 128 tokens of each linear quantized both ways, W quantized in full, {rows} rows of fprop, "
-              f"dgrad and wgrad per linear; single-threaded C oracle")
+    note = sample_note(feats, rows)
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 partial sums, f32 promotion",
-        "data": "synthetic", "config": {"workload": wl.name, "parallelism": "single host thread"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 block sums, f32 promotion",
+        "data": "synthetic", "config": {"workload": wl.name, "parallelism": "one host thread (rank 0)",
+                                        "sample_per_step": note},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": note},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -416,12 +481,14 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--cpu-rows", type=int, default=16)
-    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--cpu-feats", type=int, default=1 << 20, help="output features per linear in the CPU sample")
+    ap.add_argument("--cpu-rows", type=int, default=128)
+    ap.add_argument("--ref-feats", type=int, default=1024)
+    ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
