@@ -116,9 +116,11 @@ int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows,
                 cudaStream_t st) {
     using namespace gemm;
     using T = Tile<BN>;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
     if (!tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kc, rows, kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kc, cols, kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kc, cols, kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, cols, rows, cols * 2, 64, 32,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
         return FP8BS_ERR_LAUNCH;
 
     Params p;
@@ -147,7 +149,7 @@ int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows,
             return launch_status();
         d->gemm_attr_set[SBMODE] = true;
     }
-    kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(tmA, tmB, p);
+    kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(tmA, tmB, tmC, p);
     g_launches.fetch_add(1);
     return launch_status();
 }

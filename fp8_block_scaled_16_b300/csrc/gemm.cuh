@@ -72,7 +72,7 @@ struct Tile {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;    // 4
+    static constexpr int STAGES = 3;
     static constexpr int SA_FLOATS = BM;
     static constexpr int SB_FLOATS = BN;
     static constexpr int SLOT_FLOATS = SA_FLOATS + SB_FLOATS;
@@ -80,13 +80,18 @@ struct Tile {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SCALE = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_BAR = OFF_SCALE + SSLOTS * SLOT_FLOATS * 4;
+    // Output staging for the TMA store: per epilogue warp two 32-row x
+    // 64-column BF16 boxes (4 KB each, 128-byte swizzle).
+    static constexpr int OUT_BOX_BYTES = 32 * 64 * 2;
+    static constexpr int OFF_OUT = (OFF_SCALE + SSLOTS * SLOT_FLOATS * 4 + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_OUT + NUM_EPI_WARPS * 2 * OUT_BOX_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 2 * SSLOTS;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment for 128-byte swizzle");
     static_assert(COLS == 128, "epilogue chunking assumes 128 columns per warp");
+    static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
     // barrier indices
     static __device__ __forceinline__ uint32_t full(int s) { return s; }
     static __device__ __forceinline__ uint32_t empty(int s) { return STAGES + s; }
@@ -189,7 +194,8 @@ __device__ __forceinline__ void promote(float (&acc)[N], int base, const uint32_
 
 template <int SBMODE, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const Params p) {
     using T = Tile<BN>;
     constexpr int STAGES = T::STAGES, NBUF = T::NBUF, COLS = T::COLS;
     extern __shared__ uint8_t smem_raw[];
@@ -220,6 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&misc[0]), TMEM_COLS);
@@ -403,19 +410,41 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) break;
             if (jvalid) {
-                uint16_t* orow = p.out + (static_cast<int64_t>(mb) * BM + row) * p.cols +
-                                 static_cast<int64_t>(nb) * BN + half * COLS;
+                // BF16 out through shared memory and two TMA stores (32 rows x 64
+                // columns each) per warp.  The 128-byte swizzle puts the 16-byte
+                // chunk c of row r at chunk c ^ (r % 8), so the 32 lanes' row
+                // writes spread over all banks.
+                const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
+                if (lane == 0) bulk_wait_read_all();  // the previous tile's stores have read the buffer
+                __syncwarp();
 #pragma unroll
-                for (int j = 0; j < COLS; j += 8) {
-                    uint4 v;
-                    v.x = f32x2_to_bf16x2(acc[j + 0], acc[j + 1]);
-                    v.y = f32x2_to_bf16x2(acc[j + 2], acc[j + 3]);
-                    v.z = f32x2_to_bf16x2(acc[j + 4], acc[j + 5]);
-                    v.w = f32x2_to_bf16x2(acc[j + 6], acc[j + 7]);
-                    *reinterpret_cast<uint4*>(orow + j) = v;
+                for (int b = 0; b < 2; b++) {
+#pragma unroll
+                    for (int c = 0; c < 8; c++) {
+                        const int j = b * 64 + c * 8;
+                        const uint32_t w0 = f32x2_to_bf16x2(acc[j + 0], acc[j + 1]);
+                        const uint32_t w1 = f32x2_to_bf16x2(acc[j + 2], acc[j + 3]);
+                        const uint32_t w2 = f32x2_to_bf16x2(acc[j + 4], acc[j + 5]);
+                        const uint32_t w3 = f32x2_to_bf16x2(acc[j + 6], acc[j + 7]);
+                        const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
+                                                                             ((c ^ (lane & 7)) << 4));
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1),
+                                     "r"(w2), "r"(w3)
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int32_t x0 = nb * BN + half * COLS, y0 = mb * BM + quad * 32;
+                    tma_store_2d(&tmC, stage_out, x0, y0);
+                    tma_store_2d(&tmC, stage_out + T::OUT_BOX_BYTES, x0 + 64, y0);
+                    bulk_commit_group();
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
