@@ -323,6 +323,33 @@ def stored_traffic(kernel, workload):
         return None
 
 
+def bf16_comparison(wl, steps_data, steps=10, warmup=3):
+    """The same step's twelve GEMMs in plain BF16 through torch.matmul
+    (cuBLAS), no quantization: a comparison for the FP8 path's speed-up, the
+    B300 counterpart of the pages' FP8-vs-BF16 training-throughput ratio.
+    Not part of the measured path."""
+    mats = []
+    for (st, d), lin in zip(steps_data, wl.linears):
+        x, w, dy = d["x"], d["w"], d.get("dy")
+        mats.append(lambda x=x, w=w: torch.matmul(x, w.t()))
+        if "dgrad" in lin.ops:
+            mats.append(lambda dy=dy, w=w: torch.matmul(dy, w))
+        if "wgrad" in lin.ops:
+            mats.append(lambda dy=dy, x=x: torch.matmul(dy.t(), x))
+    for _ in range(warmup):
+        for f in mats:
+            f()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        for f in mats:
+            f()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def run_ours(args):
     from fp8_block_scaled_16_b300 import binding as B
     from fp8_block_scaled_16_b300.linear import Fp8LinearStep
@@ -431,6 +458,12 @@ def run_ours(args):
         result["cpu_baseline"] = {
             "value": fl / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": sample_note(args.cpu_feats, args.cpu_rows) + f", {sec:.1f} s"}
+    if ranks.world == 1 and not args.no_bf16:
+        bf_ms = bf16_comparison(wl, steps_data)
+        result["bf16_comparison"] = {
+            "ms_per_step": round(bf_ms, 4), "TFLOP/s": round(flops_step / (bf_ms * 1e-3) / 1e12, 1),
+            "fp8_step_speedup": round(bf_ms / ms_max, 3),
+            "note": "the step's twelve GEMMs in BF16 via torch.matmul (cuBLAS), no quantization; comparison only"}
     if ranks.world == 1 and not args.no_sweep:
         result["per_workload"] = sweep(peaks, fp8_burst)
     if ranks.rank == 0:
@@ -492,6 +525,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
