@@ -37,6 +37,8 @@ SIGNATURES = {
     "fp8bs_gemm_dgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_gemm_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_get_device_status": (ctypes.c_int, [_P]),
+    "fp8bs_set_workspace": (ctypes.c_int, [_P, _I64]),
+    "fp8bs_gemm_wgrad_workspace_bytes": (_I64, [_I64, _I64, _I64]),
     "fp8bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8bs_launch_count": (_I64, []),
     "fp8bs_debug_set_wait_timeout_ns": (ctypes.c_int, [_I64]),
@@ -174,10 +176,50 @@ def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None) -> torch.Tensor:
     return dx
 
 
-def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None) -> torch.Tensor:
-    """dW [N][K] BF16 = dY^T X from dYTq [N][M], sdyT [M/128][N], XTq [K][M], sxT [M/128][K]."""
+_workspaces = {}  # device index -> registered scratch tensor
+
+
+def _ensure_workspace(M: int, N: int, K: int, device) -> None:
+    """Registers (torch-allocated) scratch for the weight gradient's split-K
+    path if this shape would use more than the device has registered.  A
+    new buffer replaces the old one only after the device is idle."""
+    need = int(load().fp8bs_gemm_wgrad_workspace_bytes(M, N, K))
+    if need <= 0:
+        return
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    cur = _workspaces.get(idx)
+    if cur is not None and cur.numel() >= need:
+        return
+    with torch.cuda.device(idx):
+        torch.cuda.synchronize()
+        buf = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", idx))
+        _check(load().fp8bs_set_workspace(buf.data_ptr(), need), "fp8bs_set_workspace")
+    _workspaces[idx] = buf
+
+
+def fp8bs_set_workspace(ws: Optional[torch.Tensor]) -> None:
+    """Registers a uint8 CUDA tensor as the current device's scratch (None
+    unregisters)."""
+    if ws is None:
+        _check(load().fp8bs_set_workspace(None, 0), "fp8bs_set_workspace")
+        _workspaces.pop(torch.cuda.current_device(), None)
+        return
+    _check(load().fp8bs_set_workspace(_dev(ws, torch.uint8, (ws.numel(),), "ws"), ws.numel()),
+           "fp8bs_set_workspace")
+    _workspaces[ws.device.index] = ws
+
+
+def fp8bs_gemm_wgrad_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().fp8bs_gemm_wgrad_workspace_bytes(M, N, K))
+
+
+def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None, split=True) -> torch.Tensor:
+    """dW [N][K] BF16 = dY^T X from dYTq [N][M], sdyT [M/128][N], XTq [K][M], sxT [M/128][K].
+    With split=True the binding makes sure split-K scratch is registered."""
     N, M = dyTq.shape
     K = xTq.shape[0]
+    if split:
+        _ensure_workspace(M, N, K, dyTq.device)
     dw = _out(dw, (N, K), torch.bfloat16, dyTq.device)
     _check(load().fp8bs_gemm_wgrad(
         _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),

@@ -34,6 +34,10 @@ struct DeviceInfo {
     int sm_count = 0;
     uint32_t* status = nullptr;
     bool gemm_attr_set[2] = {false, false};
+    // Caller-registered scratch for split-K weight gradients (fp8bs_set_workspace).
+    uint8_t* ws = nullptr;
+    int64_t ws_bytes = 0;
+    std::atomic<uint32_t> epoch{0};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -110,6 +114,35 @@ int launch_status() {
     return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
+// Split-K plan for a weight gradient: the number of K splits per output tile
+// that fills the last wave of a persistent launch noticeably better (at
+// least 5 points of SM occupancy) than fewer splits, with at least 16 K
+// blocks per split and the split flags within the fixed flag region.
+constexpr int64_t kFlagBytes = 64 * 1024;         // flag region at the start of the scratch
+constexpr int64_t kPartialBytes = 128 * 256 * 4;  // one tile's FP32 partial
+struct SplitPlan {
+    int splits;
+    int64_t bytes;  // scratch needed (0 without splitting)
+};
+SplitPlan plan_splits(int64_t tiles, int64_t kblocks, int sms) {
+    auto eff = [&](int64_t units) {
+        const int64_t waves = (units + sms - 1) / sms;
+        return static_cast<double>(units) / static_cast<double>(waves * sms);
+    };
+    SplitPlan best{1, 0};
+    double best_eff = eff(tiles);
+    for (int sp = 2; sp <= 4; sp++) {
+        if (kblocks % sp != 0 || kblocks / sp < 16) continue;
+        if ((sp - 1) * tiles * gemm::NUM_EPI_WARPS * 4 > kFlagBytes) continue;
+        const double e = eff(tiles * sp);
+        if (e > best_eff + 0.05) {
+            best = {sp, kFlagBytes + (sp - 1) * tiles * kPartialBytes};
+            best_eff = e;
+        }
+    }
+    return best;
+}
+
 template <int SBMODE, int BN>
 int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
                 const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
@@ -138,10 +171,24 @@ int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows,
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
     p.fault = g_fault.exchange(0);
+    p.splits = 1;
+    p.ws = nullptr;
+    p.flags = nullptr;
+    p.epoch = 0;
 
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
-    const int grid = static_cast<int>(tiles < d->sm_count ? tiles : d->sm_count);
+    if (SBMODE == SB_VECTOR && d->ws != nullptr) {
+        const SplitPlan sp = plan_splits(tiles, p.kblocks, d->sm_count);
+        if (sp.splits > 1 && sp.bytes <= d->ws_bytes) {
+            p.splits = sp.splits;
+            p.flags = reinterpret_cast<uint32_t*>(d->ws);
+            p.ws = reinterpret_cast<float*>(d->ws + kFlagBytes);
+            p.epoch = d->epoch.fetch_add(1) + 1;
+        }
+    }
+    const int64_t units = tiles * p.splits;
+    const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
 
     auto kern = gemm_kernel<SBMODE, BN>;
     if (!d->gemm_attr_set[SBMODE]) {
@@ -245,6 +292,33 @@ int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq,
     // A = dYTq [N][M] (row scales sdyT [M/128][N]); B = XTq [K][M] with a
     // per-column scale vector sxT [M/128][K].
     return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, M, sdyT, sxT, 0, 0, dw, static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_set_workspace(void* ws, int64_t bytes) {
+    if (bytes < 0 || (ws == nullptr && bytes != 0) || (ws != nullptr && bytes < kFlagBytes))
+        return FP8BS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FP8BS_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    if (ws != nullptr && cudaMemset(ws, 0, kFlagBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    d->ws = static_cast<uint8_t*>(ws);
+    d->ws_bytes = bytes;
+    d->epoch.store(0);
+    return FP8BS_OK;
+}
+
+int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return -FP8BS_ERR_SHAPE;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return -rc;
+    const int64_t tiles = (N / gemm::BM) * ((K + 255) / 256);
+    return plan_splits(tiles, M / gemm::BK, d->sm_count).bytes;
 }
 
 int fp8bs_get_device_status(void* stream) {

@@ -113,7 +113,56 @@ struct Params {
     uint32_t* status;
     uint64_t timeout_ns;
     int32_t fault;                // test hook: withhold CTA 0's first operand copy
+    // K splits per tile (weight gradient; 1 = none).  Split s > 0 of tile t is
+    // a helper that leaves its FP32 partial in ws slot (s-1)*tiles + t and
+    // sets flags[slot*8 + warp] = epoch; split 0 is the owner that adds the
+    // helpers' partials, in split order, before it stores the tile.
+    int32_t splits;
+    float* ws;                    // [(splits-1)*tiles][8 warps][32 float4][32 lanes]
+    uint32_t* flags;              // [(splits-1)*tiles][8]
+    uint32_t epoch;
 };
+
+// One unit of work: K blocks [kb0, kb1) of output tile t, split s.  Units
+// of every split s > 0 (helpers) are numbered before all owners (s == 0),
+// so a CTA, which takes its units in increasing order, has finished all of
+// its helper units before it can wait on anyone; helpers never wait.
+struct Unit {
+    int t, s, kb0, kb1;
+};
+__device__ __forceinline__ Unit unit_of(int u, const Params& p, int num_tiles) {
+    Unit w;
+    const int helpers = (p.splits - 1) * num_tiles;
+    if (u < helpers) {
+        w.s = 1 + u / num_tiles;
+        w.t = u - (w.s - 1) * num_tiles;
+    } else {
+        w.s = 0;
+        w.t = u - helpers;
+    }
+    const int per = p.kblocks / p.splits;
+    w.kb0 = w.s * per;
+    w.kb1 = w.kb0 + per;
+    return w;
+}
+
+// Waits (bounded) until a helper's flag carries this launch's epoch.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, const WaitCtx& w) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v == epoch) return true;
+        if (*w.abort_flag) return false;
+        if (global_timer_ns() - t0 > w.timeout_ns) {
+            *w.abort_flag = 1u;
+            atomicOr(w.status, kStatusTimeout);
+            __threadfence();
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
 
 // Bounded wait used while tearing down after an abort: ignores the abort
 // flag, only the time limit ends it.
@@ -239,7 +288,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = misc[0];
     const WaitCtx wc{reinterpret_cast<volatile uint32_t*>(&misc[1]), p.status, p.timeout_ns};
     const int num_tiles = p.m_tiles * p.n_tiles;
-    const int kblocks = p.kblocks;
+    const int num_units = num_tiles * p.splits;
 
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
@@ -254,11 +303,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         uint32_t armed = 0, armed_par = 0, inj = 0;      // per stage
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
-            for (int kb = 0; kb < kblocks; kb++) {
+        for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+            const Unit w = unit_of(u, p, num_tiles);
+            const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
+            for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::empty(stage)), ph ^ 1u, wc)) { ok = false; break; }
-                const bool inject = p.fault != 0 && blockIdx.x == 0 && t == static_cast<int>(blockIdx.x) && kb == 0;
+                const bool inject = p.fault != 0 && blockIdx.x == 0 && u == static_cast<int>(blockIdx.x) && kb == w.kb0;
                 if (lane == 0) {
                     const uint32_t fb = bar(T::full(stage));
                     mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
@@ -289,8 +339,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true, issued = false;
         int last_tb = 0;
         uint32_t last_tph = 0;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            for (int kb = 0; kb < kblocks; kb++) {
+        for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+            const Unit w = unit_of(u, p, num_tiles);
+            for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
                 if (!warp_wait_bounded(bar(T::full(stage)), ph, wc)) { ok = false; break; }
                 tc_fence_after();
@@ -321,9 +372,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t sph = 0;
         bool ok = true;
         const uint32_t ring = sbase + T::OFF_SCALE;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
-            for (int kb = 0; kb < kblocks; kb++) {
+        for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+            const Unit w = unit_of(u, p, num_tiles);
+            const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
+            for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::sempty(slot)), sph ^ 1u, wc)) { ok = false; break; }
                 const uint32_t dst = ring + static_cast<uint32_t>(slot * T::SLOT_FLOATS * 4);
                 cp_async_16(dst + lane * 16, p.sa + static_cast<int64_t>(kb) * p.rows + mb * BM + lane * 4);
@@ -355,8 +407,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         int tb = 0, slot = 0;
         uint32_t tph = 0, sph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const int mb = t / p.n_tiles, nb = t - mb * p.n_tiles;
+        for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+            const Unit w = unit_of(u, p, num_tiles);
+            const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
             // 128-column block of the output this warp's columns fall in
             const int jb = (nb * BN + half * COLS) >> 7;
             const bool jvalid = jb < p.nb_valid;
@@ -364,10 +417,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = 0; i < COLS; i++) acc[i] = 0.0f;
             float sb_next = 0.0f;
-            if (SBMODE == SB_SCALAR && jvalid) sb_next = __ldg(p.sb + jb * p.sb_stride_j);
-            for (int kb = 0; kb < kblocks; kb++) {
+            if (SBMODE == SB_SCALAR && jvalid) sb_next = __ldg(p.sb + jb * p.sb_stride_j + w.kb0 * p.sb_stride_b);
+            for (int kb = w.kb0; kb < w.kb1; kb++) {
                 const float sb_cur = sb_next;
-                if (SBMODE == SB_SCALAR && jvalid && kb + 1 < kblocks)
+                if (SBMODE == SB_SCALAR && jvalid && kb + 1 < w.kb1)
                     sb_next = __ldg(p.sb + jb * p.sb_stride_j + (kb + 1) * p.sb_stride_b);
                 if (!warp_wait_bounded(bar(T::sfull(slot)), sph, wc)) { ok = false; break; }
                 const float* sl = ring + slot * T::SLOT_FLOATS;
@@ -409,6 +462,41 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
             }
             if (!ok) break;
+            if constexpr (SBMODE == SB_VECTOR) {
+                if (w.s > 0) {
+                    // Helper: publish this warp's FP32 partial (lane-interleaved float4s,
+                    // so every store instruction writes 512 contiguous bytes), then the flag.
+                    const int slot_id = (w.s - 1) * num_tiles + w.t;
+                    float4* dst = reinterpret_cast<float4*>(p.ws) + (static_cast<int64_t>(slot_id) * NUM_EPI_WARPS + ew) * 1024;
+#pragma unroll
+                    for (int c = 0; c < 32; c++)
+                        dst[c * 32 + lane] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0)
+                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + slot_id * NUM_EPI_WARPS + ew),
+                                     "r"(p.epoch)
+                                     : "memory");
+                    continue;
+                }
+                // Owner: add the helpers' partials in split order.
+                for (int j = 1; ok && j < p.splits; j++) {
+                    const int slot_id = (j - 1) * num_tiles + w.t;
+                    const bool got = wait_flag(p.flags + slot_id * NUM_EPI_WARPS + ew, p.epoch, wc);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    const float4* src =
+                        reinterpret_cast<const float4*>(p.ws) + (static_cast<int64_t>(slot_id) * NUM_EPI_WARPS + ew) * 1024;
+#pragma unroll
+                    for (int c = 0; c < 32; c++) {
+                        const float4 v = __ldcg(src + c * 32 + lane);
+                        acc[4 * c] += v.x;
+                        acc[4 * c + 1] += v.y;
+                        acc[4 * c + 2] += v.z;
+                        acc[4 * c + 3] += v.w;
+                    }
+                }
+                if (!ok) break;
+            }
             if (jvalid) {
                 // BF16 out through shared memory and two TMA stores (32 rows x 64
                 // columns each) per warp.  The 128-byte swizzle puts the 16-byte

@@ -129,10 +129,38 @@ int fp8bs_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, c
  *        COLWISE_T), xTq [K][M] E4M3 with sxT [M/128][K] (the same on X).
  *   dW[n][k] = bf16( fma-chain over token blocks b of
  *              P_b[n][k] * (sdyT[b][n] * sxT[b][k]) ).
+ * With a registered scratch buffer (fp8bs_set_workspace) the contraction
+ * may be split across CTAs; see there.
  * Passage: as for fprop.
  */
 int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
                      void* dw, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Scratch memory for the weight gradient's split-K path (caller-owned).
+ *
+ * When a weight gradient has few output tiles (e.g. 2048 x 5632 outputs on
+ * 148 SMs), fp8bs_gemm_wgrad splits the token contraction of each tile into
+ * 2-4 parts computed by different CTAs; the parts' FP32 partial sums are
+ * added in a fixed order (split 0 + split 1 + ...), so results stay
+ * bitwise deterministic, and each part keeps the per-128-token promotion
+ * chain.  The partial sums go through this scratch buffer:
+ *
+ *   fp8bs_gemm_wgrad_workspace_bytes(M, N, K): bytes the current device
+ *     needs for a weight gradient of that shape; 0 if it would not split;
+ *     a negative status on bad shapes or no usable device.
+ *   fp8bs_set_workspace(ws, bytes): registers `bytes` of DEVICE memory at
+ *     `ws` (256-byte aligned, bytes >= 64 KiB; NULL and 0 unregister) as the
+ *     current device's scratch.  The library zeroes its first 64 KiB (the
+ *     completion flags) with a blocking cudaMemset and keeps the pointer; the
+ *     caller keeps the memory alive and unmodified while it is registered,
+ *     and registers only while no weight gradient is running.  Without a
+ *     large enough registration the weight gradient simply does not split.
+ *     Weight gradients that share one scratch must not overlap in time (two
+ *     streams would race on it).
+ */
+int fp8bs_set_workspace(void* ws, int64_t bytes);
+int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Synchronizes `stream`, then returns and clears the current device's
  * status word: FP8BS_OK, FP8BS_ERR_TIMEOUT (a kernel gave up a bounded

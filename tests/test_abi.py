@@ -76,6 +76,12 @@ def test_validation_before_launch(lib):
     assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, None, None) == 1
     assert lib.fp8bs_debug_e4m3_encode_bits(0xFFFFFFF0, 32, fake, None) == 2
     assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, odd, None) == 3
+    assert lib.fp8bs_set_workspace(None, 5) == 1
+    assert lib.fp8bs_set_workspace(fake, -1) == 1
+    assert lib.fp8bs_set_workspace(fake, 1000) == 1               # below the 64 KiB flag region
+    assert lib.fp8bs_set_workspace(ctypes.c_void_p(0x10010), 1 << 20) == 3
+    assert lib.fp8bs_gemm_wgrad_workspace_bytes(100, 128, 128) == -2
+    assert lib.fp8bs_gemm_wgrad_workspace_bytes(128, 0, 128) == -2
 
 
 def test_debug_setters(lib):

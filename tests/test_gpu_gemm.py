@@ -147,6 +147,33 @@ def test_deterministic():
         assert torch.equal(u.view(torch.int16), v.view(torch.int16))
 
 
+def test_wgrad_split_k_is_deterministic_and_within_tolerance():
+    """A weight gradient with few output tiles (2048 x 5632 -> 352 tiles of
+    128 x 256 on 148 SMs) is split along the tokens; the split partials are
+    added in a fixed order, so repeated runs are bitwise identical, and the
+    result meets the acceptance rule like the unsplit one."""
+    M, N, K = 8192, 2048, 5632
+    assert B.fp8bs_gemm_wgrad_workspace_bytes(M, N, K) > 0, "this shape should split"
+    x = inputs.random_bf16((M, K), seed=41)
+    dy = inputs.random_bf16((M, N), seed=42, std=1e-3)
+    _, _, xTq, sxT = B.fp8bs_quantize_act(x.cuda(), B.COLWISE_T)
+    _, _, dyTq, sdyT = B.fp8bs_quantize_act(dy.cuda(), B.COLWISE_T)
+    runs = [B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT).view(torch.int16).clone() for _ in range(5)]
+    assert B.fp8bs_get_device_status() == 0
+    for r in runs[1:]:
+        assert torch.equal(r, runs[0])
+    B.fp8bs_set_workspace(None)  # no scratch registered: the same call does not split
+    unsplit = B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, split=False)
+    assert B.fp8bs_get_device_status() == 0
+    rows = inputs.sample_rows(N, 4242, 256).numpy()
+    oxTq, osxT = oracle.quant_colwise_128x1_T(x)
+    odyTq, osdyT = oracle.quant_colwise_128x1_T(dy)
+    acc, _, sab = oracle_gemm_rows("wgrad", odyTq, osdyT, oxTq, osxT, rows)
+    split_bits = runs[0].cpu().numpy().view(np.uint16)[rows]
+    assert_gemm_close(split_bits, acc, sab, "split wgrad")
+    assert_gemm_close(np_bf16_bits(unsplit)[rows], acc, sab, "unsplit wgrad")
+
+
 def test_bounded_wait_reports_timeout_and_gpu_stays_usable():
     """A withheld operand copy makes one CTA's MMA wait run out: the kernel
     records FP8BS_ERR_TIMEOUT and returns (no trap, no hang); the next
