@@ -39,6 +39,7 @@ SIGNATURES = {
     "fp8bs_get_device_status": (ctypes.c_int, [_P]),
     "fp8bs_set_workspace": (ctypes.c_int, [_P, _I64]),
     "fp8bs_gemm_wgrad_workspace_bytes": (_I64, [_I64, _I64, _I64]),
+    "fp8bs_gemm_wgrad_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8bs_launch_count": (_I64, []),
     "fp8bs_debug_set_wait_timeout_ns": (ctypes.c_int, [_I64]),
@@ -225,6 +226,20 @@ def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None, split=True) -> 
         _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
         _dev(xTq, torch.uint8, (K, M), "xTq"), _dev(sxT, torch.float32, (M // 128, K), "sxT"),
         _dev(dw, torch.bfloat16, (N, K), "dw"), M, N, K, _stream(stream)), "fp8bs_gemm_wgrad")
+    return dw
+
+
+def fp8bs_gemm_wgrad_noalloc(dyTq, sdyT, xTq, sxT, dw=None, stream=None) -> torch.Tensor:
+    """As fp8bs_gemm_wgrad, but the library takes its split-K scratch from a
+    static device array instead of registered memory (for callers that
+    cannot allocate); shapes that need more scratch raise Fp8bsError."""
+    N, M = dyTq.shape
+    K = xTq.shape[0]
+    dw = _out(dw, (N, K), torch.bfloat16, dyTq.device)
+    _check(load().fp8bs_gemm_wgrad_noalloc(
+        _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
+        _dev(xTq, torch.uint8, (K, M), "xTq"), _dev(sxT, torch.float32, (M // 128, K), "sxT"),
+        _dev(dw, torch.bfloat16, (N, K), "dw"), M, N, K, _stream(stream)), "fp8bs_gemm_wgrad_noalloc")
     return dw
 
 

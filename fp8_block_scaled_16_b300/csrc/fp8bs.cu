@@ -19,6 +19,13 @@ namespace fp8bs {
 // Per-device status word written by kernels that give up a bounded wait.
 __device__ uint32_t g_device_status;
 
+// Scratch of fp8bs_gemm_wgrad_noalloc: split-K flags (first 64 KiB) and FP32
+// partial sums, in static device memory that exists on every device where
+// this library's kernels are loaded, for the life of the process.  In host
+// code this name is only a handle: its device address comes from
+// cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[FP8BS_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -38,6 +45,10 @@ struct DeviceInfo {
     uint8_t* ws = nullptr;
     int64_t ws_bytes = 0;
     std::atomic<uint32_t> epoch{0};
+    // fp8bs_gemm_wgrad_noalloc: device address of g_noalloc_scratch on this
+    // device, looked up by that entry point's first call here.
+    bool noalloc_ready = false;
+    uint8_t* noalloc_scratch = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -319,6 +330,85 @@ int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (rc != FP8BS_OK) return -rc;
     const int64_t tiles = (N / gemm::BM) * ((K + 255) / 256);
     return plan_splits(tiles, M / gemm::BK, d->sm_count).bytes;
+}
+
+int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
+                             void* dw, int64_t M, int64_t N, int64_t K, void* stream) {
+    using namespace gemm;
+    using T = Tile<256>;
+    int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
+    if (rc != FP8BS_OK) return rc;
+    DeviceInfo* d = nullptr;
+    rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    {
+        // Set-up, once per device, with that device current: the device
+        // address of the static scratch.
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!d->noalloc_ready) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+                cudaGetLastError();
+                return FP8BS_ERR_CUDA;
+            }
+            d->noalloc_scratch = static_cast<uint8_t*>(ptr);
+            d->noalloc_ready = true;
+        }
+    }
+    // Same operand roles as fp8bs_gemm_wgrad: rows = N, cols = K, contraction M.
+    const int64_t rows = N, cols = K, kc = M;
+    const int64_t tiles = (rows / BM) * ((cols + 255) / 256);
+    if (tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
+    const SplitPlan sp = plan_splits(tiles, kc / BK, d->sm_count);
+    if (sp.bytes > static_cast<int64_t>(FP8BS_NOALLOC_SCRATCH_BYTES)) return FP8BS_ERR_SHAPE;
+
+    CUtensorMap tmA, tmB, tmC;
+    if (!tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, dyTq, kc, rows, kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, xTq, kc, cols, kc, BK, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dw, cols, rows, cols * 2, 64, 32,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8BS_ERR_LAUNCH;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    Params p;
+    p.m_tiles = static_cast<int32_t>(rows / BM);
+    p.n_tiles = static_cast<int32_t>((cols + 255) / 256);
+    p.kblocks = static_cast<int32_t>(kc / BK);
+    p.nb_valid = static_cast<int32_t>(cols / 128);
+    p.rows = rows;
+    p.cols = cols;
+    p.sa = sdyT;
+    p.sb = sxT;
+    p.sb_stride_j = 0;
+    p.sb_stride_b = 0;
+    p.out = static_cast<uint16_t*>(dw);
+    p.status = d->status;
+    p.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
+    p.fault = 0;
+    p.splits = sp.splits;
+    p.ws = nullptr;
+    p.flags = nullptr;
+    p.epoch = 0;
+    if (sp.splits > 1) {
+        // The scratch keeps whatever the previous call left: clear the flags
+        // this call will use (partials are always written before they are read).
+        const int64_t flag_bytes = (sp.splits - 1) * tiles * NUM_EPI_WARPS * 4;
+        if (cudaMemsetAsync(d->noalloc_scratch, 0, static_cast<size_t>(flag_bytes), st) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_LAUNCH;
+        }
+        p.flags = reinterpret_cast<uint32_t*>(d->noalloc_scratch);
+        p.ws = reinterpret_cast<float*>(d->noalloc_scratch + kFlagBytes);
+        p.epoch = 1;
+    }
+    const int64_t units = tiles * p.splits;
+    const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
+    auto kern = gemm_kernel<SB_VECTOR, 256>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
+        return launch_status();
+    kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(tmA, tmB, tmC, p);
+    g_launches.fetch_add(1);
+    return launch_status();
 }
 
 int fp8bs_get_device_status(void* stream) {

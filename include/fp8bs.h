@@ -162,6 +162,40 @@ int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq,
 int fp8bs_set_workspace(void* ws, int64_t bytes);
 int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/*
+ * Weight gradient for callers that cannot allocate.
+ *
+ * The paper has no counterpart of this call; it exists for library users.
+ * fp8bs_gemm_wgrad needs scratch memory from its caller to split small
+ * weight gradients (fp8bs_set_workspace).  Some callers cannot provide any:
+ * code embedded in a host framework that owns all device memory through its
+ * own pool and exposes no allocator to plug-ins, or latency-critical loops
+ * in which a cudaMalloc (which can synchronize the whole device and take
+ * arbitrarily long) is not acceptable.  This entry point computes the same
+ * dW = dY^T X with the same arguments, layouts, split plan and results as
+ * fp8bs_gemm_wgrad, but takes its scratch from a static device array of
+ * FP8BS_NOALLOC_SCRATCH_BYTES (48 MiB) compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  Neither
+ * the library nor the caller allocates anything: the caller passes only the
+ * inputs and the output, as for fp8bs_gemm_wgrad.
+ *
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call outside any stream
+ *     capture.
+ *   - Shapes whose split plan needs more scratch than the array holds are
+ *     rejected with FP8BS_ERR_SHAPE before anything is launched
+ *     (fp8bs_gemm_wgrad_workspace_bytes tells the need).
+ *   - Every call on a device shares the one array; each call first clears
+ *     (cudaMemsetAsync on `stream`) the completion flags it will use.  Two
+ *     calls that may overlap on the GPU (different streams, no ordering
+ *     between them) race on the array and give wrong results.
+ *   - Errors as for fp8bs_gemm_wgrad; FP8BS_ERR_CUDA if the array's address
+ *     cannot be looked up.
+ */
+#define FP8BS_NOALLOC_SCRATCH_BYTES (48ull << 20)
+int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
+                             void* dw, int64_t M, int64_t N, int64_t K, void* stream);
+
 /* Synchronizes `stream`, then returns and clears the current device's
  * status word: FP8BS_OK, FP8BS_ERR_TIMEOUT (a kernel gave up a bounded
  * wait and returned early; its outputs are undefined), or FP8BS_ERR_CUDA
