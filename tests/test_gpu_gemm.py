@@ -209,3 +209,21 @@ def test_rejects_bad_arguments():
     assert lib.fp8bs_gemm_fprop(p, p, p, p, p, 100, 128, 128, None) == 2
     assert lib.fp8bs_gemm_wgrad(p, p, p, p, p, 128, 0, 128, None) == 2
     assert lib.fp8bs_gemm_dgrad(p + 8, p, p, p, p, 128, 128, 128, None) == 3
+
+
+def test_long_contraction_full_output():
+    """512 K blocks of promotion (K = 65536) on a small output, every
+    element against the oracle; and the weight gradient over 65536 tokens."""
+    M, N, K = 256, 512, 65536
+    x = inputs.random_bf16((M, K), seed=51)
+    w = inputs.random_bf16((N, K), seed=52, std=0.02)
+    check_linear(x, w, None, ("fprop",), 51)
+    Mt, Nt, Kt = 65536, 256, 256
+    xt = inputs.random_bf16((Mt, Kt), seed=53)
+    dyt = inputs.random_bf16((Mt, Nt), seed=54, std=1e-3)
+    _, _, xTq, sxT = B.fp8bs_quantize_act(xt.cuda(), B.COLWISE_T)
+    _, _, dyTq, sdyT = B.fp8bs_quantize_act(dyt.cuda(), B.COLWISE_T)
+    dw = B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT)
+    assert B.fp8bs_get_device_status() == 0
+    acc, _, sab = oracle_gemm_rows("wgrad", np_u8(dyTq), np_f32(sdyT), np_u8(xTq), np_f32(sxT), np.arange(Nt))
+    assert_gemm_close(np_bf16_bits(dw), acc, sab, "wgrad over 65536 tokens")

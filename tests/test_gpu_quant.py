@@ -145,3 +145,28 @@ def test_deterministic_and_rejects_bad_arguments():
     assert lib.fp8bs_quantize_act(x.data_ptr() + 2, 256, 256, 1, a[0].data_ptr(), a[1].data_ptr(),
                                   None, None, None) == 3
     assert lib.fp8bs_quantize_act(x.data_ptr(), 256, 256, 0, None, None, None, None, None) == 1
+
+
+def test_largest_grid_checked_by_row_block_slices():
+    """The largest activation the launch geometry allows (65535 row blocks of
+    128 tokens, one 128-column block: 2.1 GB of BF16).  Quantization is local
+    to each 128x128 tile, so any row block of the output must equal the
+    oracle run on that row block alone: the first, the last and some seeded
+    ones in between are checked, in both layouts."""
+    rows, cols = 65535 * 128, 128
+    g = torch.Generator(device="cuda").manual_seed(77)
+    x = torch.randn(rows, cols, generator=g, device="cuda").to(torch.bfloat16)
+    x[:, 5] *= 40.0
+    q, s, qT, sT = B.fp8bs_quantize_act(x, B.ROWWISE | B.COLWISE_T)
+    torch.cuda.synchronize()
+    blocks = [0, 1, 65534] + inputs.sample_rows(65535, 99, 13).tolist()
+    for b in sorted(set(blocks)):
+        xs = x[b * 128:(b + 1) * 128].cpu()
+        oq, os_ = oracle.quant_rowwise_1x128(xs)
+        oqT, osT = oracle.quant_colwise_128x1_T(xs)
+        assert np.array_equal(np_u8(q[b * 128:(b + 1) * 128]), oq), b
+        assert np.array_equal(np_f32(s[:, b * 128:(b + 1) * 128]).view(np.uint32), os_.view(np.uint32)), b
+        assert np.array_equal(np_u8(qT[:, b * 128:(b + 1) * 128]), oqT), b
+        assert np.array_equal(np_f32(sT[b:b + 1]).view(np.uint32), osT.view(np.uint32)), b
+    del x, q, s, qT, sT
+    torch.cuda.empty_cache()
