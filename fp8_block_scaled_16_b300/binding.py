@@ -40,6 +40,7 @@ SIGNATURES = {
     "fp8bs_set_workspace": (ctypes.c_int, [_P, _I64]),
     "fp8bs_gemm_wgrad_workspace_bytes": (_I64, [_I64, _I64, _I64]),
     "fp8bs_gemm_wgrad_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8bs_gemm_wgrad_accumulate_f32": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8bs_launch_count": (_I64, []),
     "fp8bs_debug_set_wait_timeout_ns": (ctypes.c_int, [_I64]),
@@ -226,6 +227,18 @@ def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None, split=True) -> 
         _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
         _dev(xTq, torch.uint8, (K, M), "xTq"), _dev(sxT, torch.float32, (M // 128, K), "sxT"),
         _dev(dw, torch.bfloat16, (N, K), "dw"), M, N, K, _stream(stream)), "fp8bs_gemm_wgrad")
+    return dw
+
+
+def fp8bs_gemm_wgrad_accumulate_f32(dyTq, sdyT, xTq, sxT, dw, stream=None) -> torch.Tensor:
+    """dW (FP32 [N][K], updated in place) += dY^T X."""
+    N, M = dyTq.shape
+    K = xTq.shape[0]
+    _ensure_workspace(M, N, K, dyTq.device)
+    _check(load().fp8bs_gemm_wgrad_accumulate_f32(
+        _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
+        _dev(xTq, torch.uint8, (K, M), "xTq"), _dev(sxT, torch.float32, (M // 128, K), "sxT"),
+        _dev(dw, torch.float32, (N, K), "dw"), M, N, K, _stream(stream)), "fp8bs_gemm_wgrad_accumulate_f32")
     return dw
 
 

@@ -157,17 +157,20 @@ SplitPlan plan_splits(int64_t tiles, int64_t kblocks, int sms) {
 template <int SBMODE, int BN>
 int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
                 const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
-                cudaStream_t st) {
+                cudaStream_t st, bool out_f32_add = false) {
     using namespace gemm;
     using T = Tile<BN>;
     CUtensorMap tmA, tmB, tmC;
     if (!tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kc, rows, kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kc, cols, kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, cols, rows, cols * 2, 64, 32,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+        !(out_f32_add ? tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, cols, rows, cols * 4, 32, 32,
+                                CU_TENSOR_MAP_SWIZZLE_128B)
+                      : tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, cols, rows, cols * 2, 64, 32,
+                                CU_TENSOR_MAP_SWIZZLE_128B)))
         return FP8BS_ERR_LAUNCH;
 
     Params p;
+    p.out_f32_add = out_f32_add ? 1 : 0;
     p.m_tiles = static_cast<int32_t>(rows / BM);
     p.n_tiles = static_cast<int32_t>((cols + BN - 1) / BN);
     p.kblocks = static_cast<int32_t>(kc / BK);
@@ -215,12 +218,13 @@ int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows,
 // C[rows][cols] = block-scaled A[rows][kc] * B[cols][kc]^T (see gemm.cuh).
 int run_gemm(int sbmode, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
              const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
-             cudaStream_t st) {
+             cudaStream_t st, bool out_f32_add = false) {
     DeviceInfo* d = nullptr;
     int rc = current_device(&d);
     if (rc != FP8BS_OK) return rc;
     if (sbmode == gemm::SB_VECTOR)
-        return launch_gemm<gemm::SB_VECTOR, 256>(d, A, B, rows, cols, kc, sa, sb, sb_stride_j, sb_stride_b, out, st);
+        return launch_gemm<gemm::SB_VECTOR, 256>(d, A, B, rows, cols, kc, sa, sb, sb_stride_j, sb_stride_b, out, st,
+                                                 out_f32_add);
     return launch_gemm<gemm::SB_SCALAR, 256>(d, A, B, rows, cols, kc, sa, sb, sb_stride_j, sb_stride_b, out, st);
 }
 
@@ -305,6 +309,14 @@ int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq,
     return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, M, sdyT, sxT, 0, 0, dw, static_cast<cudaStream_t>(stream));
 }
 
+int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
+                                    float* dw, int64_t M, int64_t N, int64_t K, void* stream) {
+    int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
+    if (rc != FP8BS_OK) return rc;
+    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, M, sdyT, sxT, 0, 0, dw, static_cast<cudaStream_t>(stream),
+                    true);
+}
+
 int fp8bs_set_workspace(void* ws, int64_t bytes) {
     if (bytes < 0 || (ws == nullptr && bytes != 0) || (ws != nullptr && bytes < kFlagBytes))
         return FP8BS_ERR_INVALID_ARG;
@@ -385,6 +397,7 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
     p.fault = 0;
+    p.out_f32_add = 0;
     p.splits = sp.splits;
     p.ws = nullptr;
     p.flags = nullptr;

@@ -117,6 +117,7 @@ struct Params {
     // a helper that leaves its FP32 partial in ws slot (s-1)*tiles + t and
     // sets flags[slot*8 + warp] = epoch; split 0 is the owner that adds the
     // helpers' partials, in split order, before it stores the tile.
+    int32_t out_f32_add;          // 0: BF16 store into out; 1: FP32 out += result (tmC is FP32)
     int32_t splits;
     float* ws;                    // [(splits-1)*tiles][8 warps][32 float4][32 lanes]
     uint32_t* flags;              // [(splits-1)*tiles][8]
@@ -497,7 +498,38 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (!ok) break;
             }
-            if (jvalid) {
+            if (jvalid && p.out_f32_add) {
+                // FP32 accumulate: four 32-row x 32-column boxes per warp, staged two
+                // at a time (same 8 KB buffer, 128-byte swizzle: 16-byte chunk c of
+                // row r at chunk c ^ (r % 8)) and added to global memory by TMA
+                // reduce-add, so each output element receives exactly one FP32 add.
+                const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int b = 0; b < 2; b++) {
+#pragma unroll
+                        for (int c = 0; c < 8; c++) {
+                            const int j = h * 64 + b * 32 + c * 4;
+                            const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
+                                                                                 ((c ^ (lane & 7)) << 4));
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(acc[j]),
+                                         "f"(acc[j + 1]), "f"(acc[j + 2]), "f"(acc[j + 3])
+                                         : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int32_t x0 = nb * BN + half * COLS + h * 64, y0 = mb * BM + quad * 32;
+                        tma_reduce_add_2d(&tmC, stage_out, x0, y0);
+                        tma_reduce_add_2d(&tmC, stage_out + T::OUT_BOX_BYTES, x0 + 32, y0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (jvalid) {
                 // BF16 out through shared memory and two TMA stores (32 rows x 64
                 // columns each) per warp.  The 128-byte swizzle puts the 16-byte
                 // chunk c of row r at chunk c ^ (r % 8), so the 32 lanes' row

@@ -137,6 +137,21 @@ int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq,
                      void* dw, int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * Weight gradient accumulated in FP32:  dW += dY^T X.
+ *   Same operands, layouts and promotion as fp8bs_gemm_wgrad, but dw is an
+ *   FP32 [N][K] buffer that the result is added to (TMA reduce-add: each
+ *   element receives one FP32 add, in stream order across calls), with no
+ *   BF16 rounding: for gradient accumulation over micro-batches in the
+ *   master-gradient precision that the training state keeps (the pages keep
+ *   master weights and optimizer state in FP32/BF16).  Uses the split-K
+ *   scratch like fp8bs_gemm_wgrad.
+ * Passage: as for fprop; "numerically sensitive operations and persistent
+ * training states ... in BF16 or FP32" (arXiv part 1/7, section 2.1).
+ */
+int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
+                                    float* dw, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * Scratch memory for the weight gradient's split-K path (caller-owned).
  *
  * When a weight gradient has few output tiles (e.g. 2048 x 5632 outputs on

@@ -174,6 +174,41 @@ def test_wgrad_split_k_is_deterministic_and_within_tolerance():
     assert_gemm_close(np_bf16_bits(unsplit)[rows], acc, sab, "unsplit wgrad")
 
 
+@pytest.mark.parametrize("M,N,K", [(384, 256, 640), (8192, 2048, 5632)])
+def test_wgrad_accumulates_in_fp32(M, N, K):
+    """dW (FP32) += dY^T X, twice, starting from random FP32 values: every
+    element equals D0 + k * acc up to the GEMM tolerance (no BF16 rounding
+    here, so the 2^-8 |ref| term is generous) plus the FP32 adds' rounding;
+    repeated from the same start it is bitwise reproducible.  The larger
+    shape takes the split-K path."""
+    x = inputs.random_bf16((M, K), seed=71)
+    dy = inputs.random_bf16((M, N), seed=72, std=1e-3)
+    _, _, xTq, sxT = B.fp8bs_quantize_act(x.cuda(), B.COLWISE_T)
+    _, _, dyTq, sdyT = B.fp8bs_quantize_act(dy.cuda(), B.COLWISE_T)
+    g = torch.Generator(device="cuda").manual_seed(73)
+    d0 = torch.randn(N, K, generator=g, device="cuda") * 1e-3
+    dw = d0.clone()
+    B.fp8bs_gemm_wgrad_accumulate_f32(dyTq, sdyT, xTq, sxT, dw)
+    once = dw.clone()
+    B.fp8bs_gemm_wgrad_accumulate_f32(dyTq, sdyT, xTq, sxT, dw)
+    assert B.fp8bs_get_device_status() == 0
+    again = d0.clone()
+    B.fp8bs_gemm_wgrad_accumulate_f32(dyTq, sdyT, xTq, sxT, again)
+    assert torch.equal(again.view(torch.int32), once.view(torch.int32))
+    rows = np.arange(N) if N * K <= 1 << 20 else inputs.sample_rows(N, 7474, 256).numpy()
+    oxTq, osxT = oracle.quant_colwise_128x1_T(x)
+    odyTq, osdyT = oracle.quant_colwise_128x1_T(dy)
+    acc, _, sab = oracle_gemm_rows("wgrad", odyTq, osdyT, oxTq, osxT, rows)
+    base = d0.cpu().numpy().astype(np.float64)[rows]
+    acc = acc.astype(np.float64)
+    for k, got in ((1, once), (2, dw)):
+        ref = base + k * acc
+        g64 = got.cpu().numpy().astype(np.float64)[rows]
+        tol = k * (2.0 ** -8 * np.abs(acc) + 1e-6 * sab) + 2.0 ** -22 * (np.abs(ref) + np.abs(base))
+        bad = np.abs(g64 - ref) > tol
+        assert not bad.any(), f"accumulate x{k}: {int(bad.sum())} elements outside tolerance"
+
+
 def test_bounded_wait_reports_timeout_and_gpu_stays_usable():
     """A withheld operand copy makes one CTA's MMA wait run out: the kernel
     records FP8BS_ERR_TIMEOUT and returns (no trap, no hang); the next
