@@ -60,8 +60,8 @@ _SIGS = {
     "orc_quant_rowwise_1x128": (None, [_P, _I, _I, _P, _P]),
     "orc_quant_colwise_128x1_T": (None, [_P, _I, _I, _P, _P]),
     "orc_quant_weight_128x128": (None, [_P, _I, _I, _P, _P, _P]),
-    "orc_gemm_fprop": (None, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
-    "orc_gemm_dgrad": (None, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "orc_gemm_fprop": (None, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "orc_gemm_dgrad": (None, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
     "orc_gemm_wgrad": (None, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "orc_e4m3_encode_array": (None, [_P, _I, _P]),
     "orc_e4m3_encode_bits": (None, [ctypes.c_uint32, _I, _P]),
@@ -131,22 +131,31 @@ def f32_to_bf16(v: float) -> int:
 
 # ---------------------------------------------------------------- quantizers
 
+def padded_tokens(rows: int) -> int:
+    """Token count rounded up to whole 128-token blocks (the leading dimension
+    of token-major arrays)."""
+    return (rows + 127) // 128 * 128
+
+
 def quant_rowwise_1x128(x):
-    """x BF16 [rows][cols] -> (q u8 [rows][cols], s f32 [cols/128][rows])."""
+    """x BF16 [rows][cols] -> (q u8 [rows][cols], s f32 [cols/128][Mp]);
+    Mp = rows rounded up to 128, padding rows' scales are 1."""
     xb = _bf16_bits(x)
     rows, cols = xb.shape
     q = np.empty((rows, cols), np.uint8)
-    s = np.empty((cols // 128, rows), np.float32)
+    s = np.empty((cols // 128, padded_tokens(rows)), np.float32)
     lib().orc_quant_rowwise_1x128(_ptr(xb), rows, cols, _ptr(q), _ptr(s))
     return q, s
 
 
 def quant_colwise_128x1_T(x):
-    """x BF16 [rows][cols] -> (qT u8 [cols][rows], sT f32 [rows/128][cols])."""
+    """x BF16 [rows][cols] -> (qT u8 [cols][Mp], sT f32 [Mp/128][cols]);
+    padding tokens have payload 0."""
     xb = _bf16_bits(x)
     rows, cols = xb.shape
-    qT = np.empty((cols, rows), np.uint8)
-    sT = np.empty((rows // 128, cols), np.float32)
+    mp = padded_tokens(rows)
+    qT = np.empty((cols, mp), np.uint8)
+    sT = np.empty((mp // 128, cols), np.float32)
     lib().orc_quant_colwise_128x1_T(_ptr(xb), rows, cols, _ptr(qT), _ptr(sT))
     return qT, sT
 
@@ -171,7 +180,7 @@ def _rows_arg(rows, total):
     return np.ascontiguousarray(rows, dtype=np.int64)
 
 
-def _gemm(fn, a, sa, b, sb, M, N, K, rows, out_len, total_rows):
+def _gemm(fn, a, sa, b, sb, M, N, K, rows, out_len, total_rows, ld=None):
     r = _rows_arg(rows, total_rows)
     acc = np.empty((r.size, out_len), np.float32)
     bf = np.empty((r.size, out_len), np.uint16)
@@ -180,7 +189,8 @@ def _gemm(fn, a, sa, b, sb, M, N, K, rows, out_len, total_rows):
     b = np.ascontiguousarray(b)
     sa = np.ascontiguousarray(sa, dtype=np.float32)
     sb = np.ascontiguousarray(sb, dtype=np.float32)
-    fn(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, _ptr(r), r.size,
+    extra = () if ld is None else (ld,)
+    fn(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, *extra, _ptr(r), r.size,
        _ptr(acc), _ptr(bf), _ptr(sab))
     return acc, bf, sab
 
@@ -190,19 +200,21 @@ def gemm_fprop(xq, sx, wq, sw, rows=None):
     the listed rows of Y ([len(rows)][N])."""
     M, K = xq.shape
     N = wq.shape[0]
-    return _gemm(lib().orc_gemm_fprop, xq, sx, wq, sw, M, N, K, rows, N, M)
+    assert sx.shape[0] == K // 128 and sx.shape[1] >= M
+    return _gemm(lib().orc_gemm_fprop, xq, sx, wq, sw, M, N, K, rows, N, M, ld=sx.shape[1])
 
 
 def gemm_dgrad(dyq, sdy, wq, sw, rows=None):
     """dX = dY W, with W given in its forward layout Wq [N][K]."""
     M, N = dyq.shape
     K = wq.shape[1]
-    return _gemm(lib().orc_gemm_dgrad, dyq, sdy, wq, sw, M, N, K, rows, K, M)
+    assert sdy.shape[0] == N // 128 and sdy.shape[1] >= M
+    return _gemm(lib().orc_gemm_dgrad, dyq, sdy, wq, sw, M, N, K, rows, K, M, ld=sdy.shape[1])
 
 
 def gemm_wgrad(dytq, sdyt, xtq, sxt, rows=None):
-    """dW = dY^T X from the token-major transposed payloads.  rows index dW's
-    rows (output features n)."""
+    """dW = dY^T X from the token-major transposed payloads ([features][Mp],
+    zero padding tokens included).  rows index dW's rows (output features n)."""
     N, M = dytq.shape
     K = xtq.shape[0]
     return _gemm(lib().orc_gemm_wgrad, dytq, sdyt, xtq, sxt, M, N, K, rows, K, N)

@@ -147,14 +147,26 @@ static void tile_scale(float amax, float* s, float* inv) {
 /* Quantizers                                                          */
 /* ------------------------------------------------------------------ */
 
+/* Token count rounded up to whole 128-token blocks.  Reading (token
+ * tails): when the number of tokens is not a multiple of 128, token-major
+ * arrays -- row scales, the transposed payload and its scales -- keep a
+ * leading dimension of Mp = this many tokens; the padding tokens count as
+ * zeros (payload 0x00, and a padding-only tile is an all-zero tile, s = 1). */
+static int64_t padded_tokens(int64_t rows) { return (rows + 127) / 128 * 128; }
+
 /* 1x128 row-wise activation quantization.
- * x: BF16 [rows][cols]; q: E4M3 [rows][cols]; s: FP32 [cols/128][rows]
- * (scale of tile (r, b) at s[b*rows + r]).  cols % 128 == 0. */
+ * x: BF16 [rows][cols]; q: E4M3 [rows][cols]; s: FP32 [cols/128][Mp]
+ * (scale of tile (r, b) at s[b*Mp + r]; rows r >= `rows` hold the all-zero
+ * tile scale 1).  cols % 128 == 0; rows > 0. */
 void orc_quant_rowwise_1x128(const uint16_t* x, int64_t rows, int64_t cols,
                              uint8_t* q, float* s) {
-    int64_t nb = cols / 128;
-    for (int64_t r = 0; r < rows; r++) {
+    int64_t nb = cols / 128, mp = padded_tokens(rows);
+    for (int64_t r = 0; r < mp; r++) {
         for (int64_t b = 0; b < nb; b++) {
+            if (r >= rows) {
+                s[b * mp + r] = 1.0f;
+                continue;
+            }
             const uint16_t* t = x + r * cols + b * 128;
             float amax = 0.0f;
             for (int i = 0; i < 128; i++) {
@@ -163,7 +175,7 @@ void orc_quant_rowwise_1x128(const uint16_t* x, int64_t rows, int64_t cols,
             }
             float sc, inv;
             tile_scale(amax, &sc, &inv);
-            s[b * rows + r] = sc;
+            s[b * mp + r] = sc;
             for (int i = 0; i < 128; i++)
                 q[r * cols + b * 128 + i] = orc_e4m3_encode(orc_bf16_to_f32(t[i]) * inv);
         }
@@ -172,26 +184,30 @@ void orc_quant_rowwise_1x128(const uint16_t* x, int64_t rows, int64_t cols,
 
 /* 128x1 token-dim quantization, written transposed (for the weight
  * gradient, which contracts over tokens).
- * x: BF16 [rows][cols]; qT: E4M3 [cols][rows]; sT: FP32 [rows/128][cols]
+ * x: BF16 [rows][cols]; qT: E4M3 [cols][Mp]; sT: FP32 [Mp/128][cols]
  * (scale of the tile (column c, token block b) at sT[b*cols + c]).
  * Reading: the transposed operand is quantized from the original BF16
- * tensor, not requantized from its 1x128 FP8 form.  rows % 128 == 0. */
+ * tensor, not requantized from its 1x128 FP8 form.  The last token block
+ * may hold fewer than 128 tokens: its amax is taken over the tokens present
+ * and the padding tokens' payload is 0x00 (see padded_tokens). */
 void orc_quant_colwise_128x1_T(const uint16_t* x, int64_t rows, int64_t cols,
                                uint8_t* qT, float* sT) {
-    int64_t nb = rows / 128;
+    int64_t mp = padded_tokens(rows), nb = mp / 128;
     for (int64_t c = 0; c < cols; c++) {
         for (int64_t b = 0; b < nb; b++) {
+            int64_t n = rows - b * 128;
+            if (n > 128) n = 128;
             float amax = 0.0f;
-            for (int i = 0; i < 128; i++) {
+            for (int64_t i = 0; i < n; i++) {
                 float a = fabsf(orc_bf16_to_f32(x[(b * 128 + i) * cols + c]));
                 if (a > amax) amax = a;
             }
             float sc, inv;
             tile_scale(amax, &sc, &inv);
             sT[b * cols + c] = sc;
-            for (int i = 0; i < 128; i++)
-                qT[c * rows + b * 128 + i] =
-                    orc_e4m3_encode(orc_bf16_to_f32(x[(b * 128 + i) * cols + c]) * inv);
+            for (int64_t i = 0; i < 128; i++)
+                qT[c * mp + b * 128 + i] =
+                    i < n ? orc_e4m3_encode(orc_bf16_to_f32(x[(b * 128 + i) * cols + c]) * inv) : 0x00;
         }
     }
 }
@@ -276,11 +292,12 @@ static void emit(float acc, double sabs, int64_t idx, float* out_f32,
 
 /* fprop: Y[m][n] = sum_b sX[b][m] * sW[n/128][b] * P_b[m][n],
  *        P_b[m][n] = sum_{k in block b} Xq[m][k] * Wq[n][k].
- * Xq [M][K], sX [K/128][M], Wq [N][K], sW [N/128][K/128].
+ * Xq [M][K], sX [K/128][ldsx] (ldsx >= M; the quantizer writes
+ * Mp = M rounded up to 128 tokens), Wq [N][K], sW [N/128][K/128].
  * Computes the rows listed in `rows` (nrows of them); output row i is
  * written at out[i*N .. i*N+N).  Any output pointer may be NULL. */
 void orc_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq,
-                    const float* sw, int64_t M, int64_t N, int64_t K,
+                    const float* sw, int64_t M, int64_t N, int64_t K, int64_t ldsx,
                     const int64_t* rows, int64_t nrows, float* out_f32,
                     uint16_t* out_bf16, double* out_sumabs) {
     int64_t kb = K / 128;
@@ -288,7 +305,7 @@ void orc_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq,
         int64_t m = rows[i];
         for (int64_t n = 0; n < N; n++) {
             double sabs;
-            float acc = block_dot(xq + m * K, wq + n * K, K, sx + m, M,
+            float acc = block_dot(xq + m * K, wq + n * K, K, sx + m, ldsx,
                                   sw + (n / 128) * kb, 1, &sabs);
             emit(acc, sabs, i * N + n, out_f32, out_bf16, out_sumabs);
         }
@@ -297,11 +314,11 @@ void orc_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq,
 
 /* dgrad: dX[m][k] = sum_b sdY[b][m] * sW[b][k/128] * P_b[m][k],
  *        P_b[m][k] = sum_{n in block b} dYq[m][n] * Wq[n][k].
- * dYq [M][N], sdY [N/128][M], Wq [N][K] (the forward payload: the oracle
+ * dYq [M][N], sdY [N/128][ldsdy], Wq [N][K] (the forward payload: the oracle
  * reads the weight in its own layout), sW [N/128][K/128].  Output rows as
  * for fprop, each of length K. */
 void orc_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wq,
-                    const float* sw, int64_t M, int64_t N, int64_t K,
+                    const float* sw, int64_t M, int64_t N, int64_t K, int64_t ldsdy,
                     const int64_t* rows, int64_t nrows, float* out_f32,
                     uint16_t* out_bf16, double* out_sumabs) {
     int64_t kb = K / 128;
@@ -312,7 +329,7 @@ void orc_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wq,
         for (int64_t i = 0; i < nrows; i++) {
             int64_t m = rows[i];
             double sabs;
-            float acc = block_dot(dyq + m * N, col, N, sdy + m, M,
+            float acc = block_dot(dyq + m * N, col, N, sdy + m, ldsdy,
                                   sw + k / 128, kb, &sabs);
             emit(acc, sabs, i * K + k, out_f32, out_bf16, out_sumabs);
         }
@@ -321,8 +338,10 @@ void orc_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wq,
 
 /* wgrad: dW[n][k] = sum_b sdYT[b][n] * sXT[b][k] * P_b[n][k],
  *        P_b[n][k] = sum_{m in block b} dYTq[n][m] * XTq[k][m].
- * dYTq [N][M], sdYT [M/128][N], XTq [K][M], sXT [M/128][K].  The rows
- * listed are output rows n; output row i has length K. */
+ * dYTq [N][M], sdYT [M/128][N], XTq [K][M], sXT [M/128][K], where M is
+ * the padded token count (the transposed quantizer's padding tokens are
+ * zeros and add nothing).  The rows listed are output rows n; output row i
+ * has length K. */
 void orc_gemm_wgrad(const uint8_t* dytq, const float* sdyt, const uint8_t* xtq,
                     const float* sxt, int64_t M, int64_t N, int64_t K,
                     const int64_t* rows, int64_t nrows, float* out_f32,

@@ -23,7 +23,7 @@ def test_hand_tile_amax_448_is_identity_scale():
     row = np.zeros(128, np.float32)
     row[: len(vals)] = vals
     q, s = oracle.quant_rowwise_1x128(bf16(row[None, :]))
-    assert s.shape == (1, 1) and s[0, 0] == 1.0
+    assert s.shape == (1, 128) and s[0, 0] == 1.0      # one row, padded to a 128-token block
     assert list(q[0, : len(codes)]) == codes
     assert np.all(q[0, len(codes):] == 0)
 
@@ -66,7 +66,8 @@ def test_scale_is_amax_over_448_and_amax_element_maps_to_448():
     q, s = oracle.quant_rowwise_1x128(x)
     xf = f32(x).reshape(64, 4, 128)
     amax = np.abs(xf).max(axis=2).astype(np.float32)          # [rows][blocks]
-    assert np.array_equal(s, (amax / np.float32(448.0)).T)    # IEEE float32 division
+    assert np.array_equal(s[:, :64], (amax / np.float32(448.0)).T)    # IEEE float32 division
+    assert np.all(s[:, 64:] == 1.0)                           # padding tokens: all-zero tiles
     qb = q.reshape(64, 4, 128)
     is_max = np.abs(xf) == amax[:, :, None]
     assert np.all((qb[is_max] & 0x7F) == 0x7E)
@@ -79,7 +80,7 @@ def test_power_of_two_equivariance():
     for j in (-7, -1, 1, 5):
         q1, s1 = oracle.quant_rowwise_1x128(x * (2.0 ** j))
         assert np.array_equal(q0, q1)
-        assert np.array_equal(s1, s0 * np.float32(2.0 ** j))
+        assert np.array_equal(s1[:, :32], s0[:, :32] * np.float32(2.0 ** j))
 
 
 def test_dequantization_error_bound():
@@ -125,3 +126,45 @@ def test_weight_blocks_transpose_and_scales():
     assert abs(float(wf[1, 72, 0, 3])) == amax[blk]
     assert np.array_equal(q[r, :128], q_row[r, :128])
     assert np.array_equal(q[r - 128 + 128, :128], q_row[r, :128])
+
+
+def test_token_tail_equals_zero_padding():
+    """Reading for token counts that are not a multiple of 128: the last
+    128x1 tile covers the tokens present and the padding tokens count as
+    zeros.  So quantizing 300 tokens must equal quantizing the same tensor
+    padded with zero tokens to 384 (row scales of padding rows are 1, the
+    padding payload is 0x00), and the partial tile's scale is numpy's amax of
+    the present tokens / 448."""
+    M, K = 300, 256
+    x = inputs.random_bf16((M, K), seed=16)
+    x[:, 3] *= 30.0
+    xp = torch.zeros(384, K, dtype=torch.bfloat16)
+    xp[:M] = x
+    q, s = oracle.quant_rowwise_1x128(x)
+    qp, sp = oracle.quant_rowwise_1x128(xp)
+    assert q.shape == (M, K) and s.shape == (2, 384)
+    assert np.array_equal(q, qp[:M])
+    assert np.array_equal(s[:, :M], sp[:, :M]) and np.all(s[:, M:] == 1.0)
+    qT, sT = oracle.quant_colwise_128x1_T(x)
+    qTp, sTp = oracle.quant_colwise_128x1_T(xp)
+    assert qT.shape == (K, 384) and sT.shape == (3, K)
+    assert np.array_equal(qT, qTp) and np.array_equal(sT, sTp)
+    assert np.all(qT[:, M:] == 0)
+    tail_amax = np.abs(f32(x[256:])).max(axis=0).astype(np.float32)     # 44 tokens
+    assert np.array_equal(sT[2], tail_amax / np.float32(448.0))
+
+
+def test_token_tail_gemm_rows_do_not_depend_on_padding():
+    M, N, K = 300, 256, 256
+    x = inputs.random_bf16((M, K), seed=17)
+    w = inputs.random_bf16((N, K), seed=18, std=0.02)
+    xq, sx = oracle.quant_rowwise_1x128(x)
+    wq, _, sw = oracle.quant_weight_128x128(w, want_t=False)
+    acc, y, _ = oracle.gemm_fprop(xq, sx, wq, sw)
+    xp = torch.zeros(384, K, dtype=torch.bfloat16)
+    xp[:M] = x
+    xqp, sxp = oracle.quant_rowwise_1x128(xp)
+    accp, yp, _ = oracle.gemm_fprop(xqp, sxp, wq, sw)
+    assert acc.shape == (M, N)
+    assert np.array_equal(acc, accp[:M]) and np.array_equal(y, yp[:M])
+    assert not accp[M:].any()
