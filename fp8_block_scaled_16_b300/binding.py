@@ -111,27 +111,33 @@ def _out(t: Optional[torch.Tensor], shape, dtype, device) -> torch.Tensor:
 
 # ---------------------------------------------------------------- entry points
 
+def padded_tokens(rows: int) -> int:
+    """Leading dimension of token-major arrays: rows rounded up to 128."""
+    return (rows + 127) // 128 * 128
+
+
 def fp8bs_quantize_act(x: torch.Tensor, flags: int = ROWWISE, q=None, s=None, qT=None, sT=None,
                        stream=None) -> Tuple[Optional[torch.Tensor], ...]:
-    """x BF16 [rows][cols] -> (q u8 [rows][cols], s f32 [cols/128][rows],
-    qT u8 [cols][rows], sT f32 [rows/128][cols]); the pair for a layout that
-    `flags` does not request is (None, None)."""
+    """x BF16 [rows][cols] -> (q u8 [rows][cols], s f32 [cols/128][Mp],
+    qT u8 [cols][Mp], sT f32 [Mp/128][cols]) with Mp = rows rounded up to 128;
+    the pair for a layout that `flags` does not request is (None, None)."""
     rows, cols = x.shape
+    mp = padded_tokens(rows)
     dev = x.device
     xp = _dev(x, torch.bfloat16, (rows, cols), "x")
     ptrs = [None, None, None, None]
     if flags & ROWWISE:
         q = _out(q, (rows, cols), torch.uint8, dev)
-        s = _out(s, (cols // 128, rows), torch.float32, dev)
+        s = _out(s, (cols // 128, mp), torch.float32, dev)
         ptrs[0] = _dev(q, torch.uint8, (rows, cols), "q")
-        ptrs[1] = _dev(s, torch.float32, (cols // 128, rows), "s")
+        ptrs[1] = _dev(s, torch.float32, (cols // 128, mp), "s")
     else:
         q = s = None
     if flags & COLWISE_T:
-        qT = _out(qT, (cols, rows), torch.uint8, dev)
-        sT = _out(sT, (rows // 128, cols), torch.float32, dev)
-        ptrs[2] = _dev(qT, torch.uint8, (cols, rows), "qT")
-        ptrs[3] = _dev(sT, torch.float32, (rows // 128, cols), "sT")
+        qT = _out(qT, (cols, mp), torch.uint8, dev)
+        sT = _out(sT, (mp // 128, cols), torch.float32, dev)
+        ptrs[2] = _dev(qT, torch.uint8, (cols, mp), "qT")
+        ptrs[3] = _dev(sT, torch.float32, (mp // 128, cols), "sT")
     else:
         qT = sT = None
     _check(load().fp8bs_quantize_act(xp, rows, cols, flags, *ptrs, _stream(stream)), "fp8bs_quantize_act")
@@ -155,24 +161,24 @@ def fp8bs_quantize_weight(w: torch.Tensor, q=None, qT=None, s=None, want_t: bool
 
 
 def fp8bs_gemm_fprop(xq, sx, wq, sw, y=None, stream=None) -> torch.Tensor:
-    """Y [M][N] BF16 = X W^T from Xq [M][K], sx [K/128][M], Wq [N][K], sw [N/128][K/128]."""
+    """Y [M][N] BF16 = X W^T from Xq [M][K], sx [K/128][Mp], Wq [N][K], sw [N/128][K/128]."""
     M, K = xq.shape
     N = wq.shape[0]
     y = _out(y, (M, N), torch.bfloat16, xq.device)
     _check(load().fp8bs_gemm_fprop(
-        _dev(xq, torch.uint8, (M, K), "xq"), _dev(sx, torch.float32, (K // 128, M), "sx"),
+        _dev(xq, torch.uint8, (M, K), "xq"), _dev(sx, torch.float32, (K // 128, padded_tokens(M)), "sx"),
         _dev(wq, torch.uint8, (N, K), "wq"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
         _dev(y, torch.bfloat16, (M, N), "y"), M, N, K, _stream(stream)), "fp8bs_gemm_fprop")
     return y
 
 
 def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None) -> torch.Tensor:
-    """dX [M][K] BF16 = dY W from dYq [M][N], sdy [N/128][M], WqT [K][N], sw [N/128][K/128]."""
+    """dX [M][K] BF16 = dY W from dYq [M][N], sdy [N/128][Mp], WqT [K][N], sw [N/128][K/128]."""
     M, N = dyq.shape
     K = wqT.shape[0]
     dx = _out(dx, (M, K), torch.bfloat16, dyq.device)
     _check(load().fp8bs_gemm_dgrad(
-        _dev(dyq, torch.uint8, (M, N), "dyq"), _dev(sdy, torch.float32, (N // 128, M), "sdy"),
+        _dev(dyq, torch.uint8, (M, N), "dyq"), _dev(sdy, torch.float32, (N // 128, padded_tokens(M)), "sdy"),
         _dev(wqT, torch.uint8, (K, N), "wqT"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
         _dev(dx, torch.bfloat16, (M, K), "dx"), M, N, K, _stream(stream)), "fp8bs_gemm_dgrad")
     return dx
@@ -216,7 +222,8 @@ def fp8bs_gemm_wgrad_workspace_bytes(M: int, N: int, K: int) -> int:
 
 
 def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None, split=True) -> torch.Tensor:
-    """dW [N][K] BF16 = dY^T X from dYTq [N][M], sdyT [M/128][N], XTq [K][M], sxT [M/128][K].
+    """dW [N][K] BF16 = dY^T X from dYTq [N][Mp], sdyT [Mp/128][N], XTq [K][Mp], sxT [Mp/128][K]
+    (Mp: the token count rounded up to 128; the padding tokens are zero payloads).
     With split=True the binding makes sure split-K scratch is registered."""
     N, M = dyTq.shape
     K = xTq.shape[0]

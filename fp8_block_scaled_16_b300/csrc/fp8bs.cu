@@ -58,6 +58,10 @@ std::once_flag g_encode_once;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dim_ok(int64_t d) { return d > 0 && (d % 128) == 0 && d <= (int64_t(1) << 31); }
+// Token counts may be any positive number; token-major arrays use them
+// rounded up to whole 128-token blocks.
+bool tokens_ok(int64_t m) { return m > 0 && m <= (int64_t(1) << 31) - 128; }
+int64_t padded_tokens(int64_t m) { return (m + 127) / 128 * 128; }
 
 // Looks up (once per device) whether this device can run the sm_103a
 // kernels, its SM count and the device address of the status word.
@@ -171,7 +175,8 @@ int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows,
 
     Params p;
     p.out_f32_add = out_f32_add ? 1 : 0;
-    p.m_tiles = static_cast<int32_t>(rows / BM);
+    p.m_tiles = static_cast<int32_t>((rows + BM - 1) / BM);
+    p.sa_ld = padded_tokens(rows);
     p.n_tiles = static_cast<int32_t>((cols + BN - 1) / BN);
     p.kblocks = static_cast<int32_t>(kc / BK);
     p.nb_valid = static_cast<int32_t>(cols / 128);
@@ -240,21 +245,22 @@ int fp8bs_quantize_act(const void* x, int64_t rows, int64_t cols, unsigned flags
     const bool row = (flags & FP8BS_ROWWISE) != 0, colt = (flags & FP8BS_COLWISE_T) != 0;
     if (!x || (flags & ~(FP8BS_ROWWISE | FP8BS_COLWISE_T)) || (!row && !colt)) return FP8BS_ERR_INVALID_ARG;
     if ((row && (!q || !s)) || (colt && (!qT || !sT))) return FP8BS_ERR_INVALID_ARG;
-    if (!dim_ok(rows) || !dim_ok(cols) || rows / 128 > 65535) return FP8BS_ERR_SHAPE;
+    if (!tokens_ok(rows) || !dim_ok(cols) || padded_tokens(rows) / 128 > 65535) return FP8BS_ERR_SHAPE;
     if (!aligned16(x) || (row && (!aligned16(q) || !aligned16(s))) || (colt && (!aligned16(qT) || !aligned16(sT))))
         return FP8BS_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     int rc = current_device(&d);
     if (rc != FP8BS_OK) return rc;
-    const dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
+    const int64_t ld = padded_tokens(rows);
+    const dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(ld / 128));
     const auto* xw = static_cast<const uint32_t*>(x);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (row && colt)
-        quant_tile_kernel<QM_ROW | QM_COLT><<<grid, 256, 0, st>>>(xw, rows, cols, q, s, qT, sT);
+        quant_tile_kernel<QM_ROW | QM_COLT><<<grid, 256, 0, st>>>(xw, rows, cols, ld, q, s, qT, sT);
     else if (row)
-        quant_tile_kernel<QM_ROW><<<grid, 256, 0, st>>>(xw, rows, cols, q, s, nullptr, nullptr);
+        quant_tile_kernel<QM_ROW><<<grid, 256, 0, st>>>(xw, rows, cols, ld, q, s, nullptr, nullptr);
     else
-        quant_tile_kernel<QM_COLT><<<grid, 256, 0, st>>>(xw, rows, cols, nullptr, nullptr, qT, sT);
+        quant_tile_kernel<QM_COLT><<<grid, 256, 0, st>>>(xw, rows, cols, ld, nullptr, nullptr, qT, sT);
     g_launches.fetch_add(1);
     return launch_status();
 }
@@ -268,7 +274,7 @@ int fp8bs_quantize_weight(const void* w, int64_t n, int64_t k, uint8_t* q, uint8
     if (rc != FP8BS_OK) return rc;
     const dim3 grid(static_cast<unsigned>(k / 128), static_cast<unsigned>(n / 128));
     quant_tile_kernel<QM_BLOCK><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint32_t*>(w), n, k, q, s, qT, nullptr);
+        static_cast<const uint32_t*>(w), n, k, n, q, s, qT, nullptr);
     g_launches.fetch_add(1);
     return launch_status();
 }
@@ -276,7 +282,7 @@ int fp8bs_quantize_weight(const void* w, int64_t n, int64_t k, uint8_t* q, uint8
 static int check_gemm_args(const void* a, const void* sa, const void* b, const void* sb, const void* out,
                            int64_t M, int64_t N, int64_t K) {
     if (!a || !sa || !b || !sb || !out) return FP8BS_ERR_INVALID_ARG;
-    if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return FP8BS_ERR_SHAPE;
+    if (!tokens_ok(M) || !dim_ok(N) || !dim_ok(K)) return FP8BS_ERR_SHAPE;
     if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out)) return FP8BS_ERR_ALIGN;
     return FP8BS_OK;
 }
@@ -306,15 +312,18 @@ int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq,
     if (rc != FP8BS_OK) return rc;
     // A = dYTq [N][M] (row scales sdyT [M/128][N]); B = XTq [K][M] with a
     // per-column scale vector sxT [M/128][K].
-    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, M, sdyT, sxT, 0, 0, dw, static_cast<cudaStream_t>(stream));
+    // Contraction over the tokens, padded to whole 128-token blocks (the
+    // transposed quantizer writes zero payloads for the padding).
+    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, padded_tokens(M), sdyT, sxT, 0, 0, dw,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
                                     float* dw, int64_t M, int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, M, sdyT, sxT, 0, 0, dw, static_cast<cudaStream_t>(stream),
-                    true);
+    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, padded_tokens(M), sdyT, sxT, 0, 0, dw,
+                    static_cast<cudaStream_t>(stream), true);
 }
 
 int fp8bs_set_workspace(void* ws, int64_t bytes) {
@@ -336,12 +345,12 @@ int fp8bs_set_workspace(void* ws, int64_t bytes) {
 }
 
 int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return -FP8BS_ERR_SHAPE;
+    if (!tokens_ok(M) || !dim_ok(N) || !dim_ok(K)) return -FP8BS_ERR_SHAPE;
     DeviceInfo* d = nullptr;
     int rc = current_device(&d);
     if (rc != FP8BS_OK) return -rc;
     const int64_t tiles = (N / gemm::BM) * ((K + 255) / 256);
-    return plan_splits(tiles, M / gemm::BK, d->sm_count).bytes;
+    return plan_splits(tiles, padded_tokens(M) / gemm::BK, d->sm_count).bytes;
 }
 
 int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
@@ -368,7 +377,7 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
         }
     }
     // Same operand roles as fp8bs_gemm_wgrad: rows = N, cols = K, contraction M.
-    const int64_t rows = N, cols = K, kc = M;
+    const int64_t rows = N, cols = K, kc = padded_tokens(M);
     const int64_t tiles = (rows / BM) * ((cols + 255) / 256);
     if (tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
     const SplitPlan sp = plan_splits(tiles, kc / BK, d->sm_count);
@@ -384,6 +393,7 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
 
     Params p;
     p.m_tiles = static_cast<int32_t>(rows / BM);
+    p.sa_ld = rows;
     p.n_tiles = static_cast<int32_t>((cols + 255) / 256);
     p.kblocks = static_cast<int32_t>(kc / BK);
     p.nb_valid = static_cast<int32_t>(cols / 128);

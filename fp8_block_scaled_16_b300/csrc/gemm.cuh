@@ -104,8 +104,9 @@ struct Tile {
 struct Params {
     int32_t m_tiles, n_tiles, kblocks;
     int32_t nb_valid;             // number of 128-column blocks of the output (cols / 128)
-    int64_t rows, cols;           // output shape
-    const float* sa;              // row scales, [kblocks][rows]
+    int64_t rows, cols;           // output shape (rows need not be a multiple of 128)
+    int64_t sa_ld;                // row-scale leading dimension: rows rounded up to 128
+    const float* sa;              // row scales, [kblocks][sa_ld]
     const float* sb;              // SB_SCALAR: scalar table, index jb * sb_stride_j + b * sb_stride_b
     int64_t sb_stride_j;          //   (jb = 128-column block of the output, b = K block)
     int64_t sb_stride_b;          // SB_VECTOR: column scales [kblocks][cols]
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::sempty(slot)), sph ^ 1u, wc)) { ok = false; break; }
                 const uint32_t dst = ring + static_cast<uint32_t>(slot * T::SLOT_FLOATS * 4);
-                cp_async_16(dst + lane * 16, p.sa + static_cast<int64_t>(kb) * p.rows + mb * BM + lane * 4);
+                cp_async_16(dst + lane * 16, p.sa + static_cast<int64_t>(kb) * p.sa_ld + mb * BM + lane * 4);
                 if constexpr (SBMODE == SB_VECTOR) {
 #pragma unroll
                     for (int c = 0; c < BN / 128; c++) {
@@ -498,7 +499,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (!ok) break;
             }
-            if (jvalid && p.out_f32_add) {
+            // Output boxes that lie wholly past the last row (a token tail) are
+            // not stored; TMA clips the rows of a partial box.
+            const bool rvalid = static_cast<int64_t>(mb) * BM + quad * 32 < p.rows;
+            if (jvalid && rvalid && p.out_f32_add) {
                 // FP32 accumulate: four 32-row x 32-column boxes per warp, staged two
                 // at a time (same 8 KB buffer, 128-byte swizzle: 16-byte chunk c of
                 // row r at chunk c ^ (r % 8)) and added to global memory by TMA
@@ -529,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         bulk_commit_group();
                     }
                 }
-            } else if (jvalid) {
+            } else if (jvalid && rvalid) {
                 // BF16 out through shared memory and two TMA stores (32 rows x 64
                 // columns each) per warp.  The 128-byte swizzle puts the 16-byte
                 // chunk c of row r at chunk c ^ (r % 8), so the 32 lanes' row

@@ -53,14 +53,16 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// x: BF16 [rows][cols] viewed as 32-bit words (two BF16 per word).
-// MODE & QM_ROW   : q [rows][cols], s [cols/128][rows]
-// MODE & QM_COLT  : qT [cols][rows], sT [rows/128][cols]
+// x: BF16 [rows][cols] viewed as 32-bit words (two BF16 per word); ld is
+// the token leading dimension of the token-major outputs, rows rounded up
+// to 128 (the grid covers ld/128 row blocks; rows past `rows` read as zeros).
+// MODE & QM_ROW   : q [rows][cols], s [cols/128][ld]
+// MODE & QM_COLT  : qT [cols][ld], sT [ld/128][cols]
 // MODE == QM_BLOCK: q [rows][cols], qT [cols][rows] (nullable),
-//                   s [rows/128][cols/128]
+//                   s [rows/128][cols/128]   (rows % 128 == 0, ld == rows)
 template <int MODE>
 __global__ void __launch_bounds__(256, 5) quant_tile_kernel(const uint32_t* __restrict__ x, int64_t rows,
-                                                            int64_t cols, uint8_t* __restrict__ q,
+                                                            int64_t cols, int64_t ld, uint8_t* __restrict__ q,
                                                             float* __restrict__ s, uint8_t* __restrict__ qT,
                                                             float* __restrict__ sT) {
     constexpr bool kRow = (MODE & QM_ROW) != 0;
@@ -81,14 +83,26 @@ __global__ void __launch_bounds__(256, 5) quant_tile_kernel(const uint32_t* __re
     const int64_t wpr = cols >> 1;  // words per row
 
     // 1. The 128x128 tile into shared memory: 2048 chunks of 16 bytes, eight
-    //    per thread, all in flight at once.
+    //    per thread, all in flight at once; rows past the end are zeros.
+    const bool full = r0 + 128 <= rows;  // every tile but a token tail's last
     {
         const uint32_t* src = x + r0 * wpr + (c0 >> 1);
         const uint32_t dst = smem_u32(tile);
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const int id = i * 256 + tid, r = id >> 4, ch = id & 15;
-            cp_async16(dst + static_cast<uint32_t>(r * 256 + ch * 16), src + r * wpr + ch * 4);
+            for (int i = 0; i < 8; i++) {
+                const int id = i * 256 + tid, r = id >> 4, ch = id & 15;
+                cp_async16(dst + static_cast<uint32_t>(r * 256 + ch * 16), src + r * wpr + ch * 4);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int id = i * 256 + tid, r = id >> 4, ch = id & 15;
+                if (r0 + r < rows)
+                    cp_async16(dst + static_cast<uint32_t>(r * 256 + ch * 16), src + r * wpr + ch * 4);
+                else
+                    *reinterpret_cast<uint4*>(&tile[r * 64 + ch * 4]) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
     }
@@ -121,7 +135,7 @@ __global__ void __launch_bounds__(256, 5) quant_tile_kernel(const uint32_t* __re
             float sc, iv;
             tile_scale(__uint_as_float(rmax[tid] << 16), sc, iv);
             rinv[tid] = iv;
-            s[static_cast<int64_t>(blockIdx.x) * rows + r0 + tid] = sc;
+            s[static_cast<int64_t>(blockIdx.x) * ld + r0 + tid] = sc;
         }
     }
     if constexpr (kColT) {
@@ -156,14 +170,18 @@ __global__ void __launch_bounds__(256, 5) quant_tile_kernel(const uint32_t* __re
     //     writes rows [16w, 16w+16), lane l owns elements [4l, 4l+4): one
     //     128-byte store per row.
     if constexpr (kRow || kBlock) {
-#pragma unroll 4
-        for (int i = 0; i < 16; i++) {
-            const int r = warp * 16 + i;
+        auto row_out = [&](int r) {
             const uint2 w2 = *reinterpret_cast<const uint2*>(&tile[r * 64 + 2 * lane]);
             const float iv = kRow ? rinv[r] : binv;
             const uint32_t lo = e4m3x2(__fmul_rn(bf16lo_to_f32(w2.x), iv), __fmul_rn(bf16hi_to_f32(w2.x), iv));
             const uint32_t hi = e4m3x2(__fmul_rn(bf16lo_to_f32(w2.y), iv), __fmul_rn(bf16hi_to_f32(w2.y), iv));
             *reinterpret_cast<uint32_t*>(q + (r0 + r) * cols + c0 + 4 * lane) = lo | (hi << 16);
+        };
+        if (full) {
+#pragma unroll 4
+            for (int i = 0; i < 16; i++) row_out(warp * 16 + i);
+        } else {
+            for (int i = 0; i < 16 && r0 + warp * 16 + i < rows; i++) row_out(warp * 16 + i);
         }
     }
 
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(256, 5) quant_tile_kernel(const uint32_t* __re
             for (int i = 0; i < 4; i++) {
                 const int id = i * 256 + tid, rr = id >> 3, part = id & 7;
                 const uint4 v = *reinterpret_cast<const uint4*>(park + rr * kStride + part * 16);
-                *reinterpret_cast<uint4*>(qT + (c0 + rr) * rows + r0 + part * 16) = v;
+                *reinterpret_cast<uint4*>(qT + (c0 + rr) * ld + r0 + part * 16) = v;
             }
         }
     }

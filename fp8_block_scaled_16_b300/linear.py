@@ -39,14 +39,15 @@ class Fp8LinearStep:
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         need_t = "wgrad" in self.ops
-        self.xq, self.sx = e((M, K), u8), e((K // 128, M), f32)
-        self.xTq, self.sxT = (e((K, M), u8), e((M // 128, K), f32)) if need_t else (None, None)
+        Mp = B.padded_tokens(M)  # token-major arrays: tokens rounded up to 128
+        self.xq, self.sx = e((M, K), u8), e((K // 128, Mp), f32)
+        self.xTq, self.sxT = (e((K, Mp), u8), e((Mp // 128, K), f32)) if need_t else (None, None)
         self.wq, self.sw = e((N, K), u8), e((N // 128, K // 128), f32)
         self.wqT = e((K, N), u8) if "dgrad" in self.ops else None
         self.y = e((M, N), bf)
         bwd = "dgrad" in self.ops or "wgrad" in self.ops
-        self.dyq, self.sdy = (e((M, N), u8), e((N // 128, M), f32)) if "dgrad" in self.ops else (None, None)
-        self.dyTq, self.sdyT = (e((N, M), u8), e((M // 128, N), f32)) if need_t else (None, None)
+        self.dyq, self.sdy = (e((M, N), u8), e((N // 128, Mp), f32)) if "dgrad" in self.ops else (None, None)
+        self.dyTq, self.sdyT = (e((N, Mp), u8), e((Mp // 128, N), f32)) if need_t else (None, None)
         self.dx = e((M, K), bf) if "dgrad" in self.ops else None
         self.dw = e((N, K), bf) if "wgrad" in self.ops else None
         self.has_bwd = bwd

@@ -30,7 +30,14 @@
  *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
  *     memory) on the current device, 16-byte aligned.  The caller owns every
  *     buffer; the library never allocates or frees per call.
- *   - Every dimension must be a positive multiple of 128.
+ *   - Feature dimensions (K, N, and both dimensions of a weight) must be
+ *     positive multiples of 128.  The token count (M, the rows of X, dY, Y,
+ *     dX) may be any positive number: token-major arrays -- row scales,
+ *     transposed payloads and their scales -- then have a leading dimension
+ *     of Mp = M rounded up to a multiple of 128.  The last 128x1 token tile
+ *     covers the tokens present; padding tokens are stored as zero payloads
+ *     (and padding rows' scales as 1), so they add nothing to a product.
+ *     Everything else is laid out exactly as for M = Mp.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     are asynchronous and stream-ordered; the host never synchronizes.
  *   - Argument errors return a status and launch nothing.  Errors that
@@ -70,14 +77,16 @@ typedef enum fp8bs_status {
  *   x      : BF16 [rows][cols], read only.
  *   flags  : FP8BS_ROWWISE and/or FP8BS_COLWISE_T (at least one).
  *   q, s   : with FP8BS_ROWWISE -- E4M3 payload [rows][cols] and FP32
- *            scales [cols/128][rows]: the scale of the tile holding
- *            x[r][128b .. 128b+127] is s[b*rows + r].  Scales are stored
+ *            scales [cols/128][Mp]: the scale of the tile holding
+ *            x[r][128b .. 128b+127] is s[b*Mp + r] (Mp: rows rounded up to
+ *            128; s is 1 for r >= rows).  Scales are stored
  *            k-block-major so that the 128 row scales of one GEMM tile are
  *            contiguous.  Ignored (may be NULL) without the flag.
  *   qT, sT : with FP8BS_COLWISE_T -- the 128x1-tiled payload written
- *            transposed, qT [cols][rows] (qT[c][r] encodes x[r][c]), and
- *            FP32 scales sT [rows/128][cols]: the scale of the tile holding
- *            x[128b .. 128b+127][c] is sT[b*cols + c].  Ignored (may be NULL)
+ *            transposed, qT [cols][Mp] (qT[c][r] encodes x[r][c]; 0 for
+ *            r >= rows), and FP32 scales sT [Mp/128][cols]: the scale of the
+ *            tile holding x[128b .. 128b+127][c] (the tokens present) is
+ *            sT[b*cols + c].  Ignored (may be NULL)
  *            without the flag.
  * rows is the token count M for X or dY; cols is K (for X) or N (for dY).
  * Passage: the pages' fine-grained (tile-wise) activation quantization,
@@ -101,7 +110,7 @@ int fp8bs_quantize_weight(const void* w, int64_t n, int64_t k, uint8_t* q, uint8
 
 /*
  * Forward GEMM  Y = X W^T  (BF16 out [M][N]).
- *   xq [M][K] E4M3 with sx [K/128][M] (from fp8bs_quantize_act, ROWWISE),
+ *   xq [M][K] E4M3 with sx [K/128][Mp] (from fp8bs_quantize_act, ROWWISE),
  *   wq [N][K] E4M3 with sw [N/128][K/128] (from fp8bs_quantize_weight).
  *   Y[m][n] = bf16( sum_b fma-chain of P_b[m][n] * (sx[b][m] * sw[n/128][b]) )
  *   with P_b the FP32 tensor-core sum over k in [128b, 128b+128).
@@ -113,7 +122,7 @@ int fp8bs_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, cons
 
 /*
  * Data-gradient GEMM  dX = dY W  (BF16 out [M][K]); contraction over N.
- *   dyq [M][N] E4M3 with sdy [N/128][M] (fp8bs_quantize_act on dY, ROWWISE),
+ *   dyq [M][N] E4M3 with sdy [N/128][Mp] (fp8bs_quantize_act on dY, ROWWISE),
  *   wqT [K][N] E4M3 (the transposed payload from fp8bs_quantize_weight),
  *   sw  [N/128][K/128] (the same weight scales as fprop; block (b, k/128)
  *       scales contraction block b of output column k).
@@ -125,8 +134,9 @@ int fp8bs_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, c
 /*
  * Weight-gradient GEMM  dW = dY^T X  (BF16 out [N][K]); contraction over
  * the M tokens.
- *   dyTq [N][M] E4M3 with sdyT [M/128][N] (fp8bs_quantize_act on dY,
- *        COLWISE_T), xTq [K][M] E4M3 with sxT [M/128][K] (the same on X).
+ *   dyTq [N][Mp] E4M3 with sdyT [Mp/128][N] (fp8bs_quantize_act on dY,
+ *        COLWISE_T), xTq [K][Mp] E4M3 with sxT [Mp/128][K] (the same on X);
+ *        M is the token count (the padding tokens contribute zero).
  *   dW[n][k] = bf16( fma-chain over token blocks b of
  *              P_b[n][k] * (sdyT[b][n] * sxT[b][k]) ).
  * With a registered scratch buffer (fp8bs_set_workspace) the contraction

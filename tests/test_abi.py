@@ -61,7 +61,8 @@ def test_validation_before_launch(lib):
     assert lib.fp8bs_quantize_act(fake, 128, 128, 0, fake, fake, None, None, None) == 1
     assert lib.fp8bs_quantize_act(fake, 128, 128, 4, fake, fake, None, None, None) == 1
     assert lib.fp8bs_quantize_act(fake, 128, 128, 2, fake, fake, None, None, None) == 1  # qT/sT missing
-    assert lib.fp8bs_quantize_act(fake, 100, 128, 1, fake, fake, None, None, None) == 2
+    assert lib.fp8bs_quantize_act(fake, 128, 100, 1, fake, fake, None, None, None) == 2   # features % 128
+    assert lib.fp8bs_quantize_act(fake, 0, 128, 1, fake, fake, None, None, None) == 2     # no tokens
     assert lib.fp8bs_quantize_act(fake, 128, -128, 1, fake, fake, None, None, None) == 2
     assert lib.fp8bs_quantize_act(fake, 128 * 65536, 128, 1, fake, fake, None, None, None) == 2
     assert lib.fp8bs_quantize_act(odd, 128, 128, 1, fake, fake, None, None, None) == 3
@@ -71,6 +72,8 @@ def test_validation_before_launch(lib):
     for fn in (lib.fp8bs_gemm_fprop, lib.fp8bs_gemm_dgrad, lib.fp8bs_gemm_wgrad):
         assert fn(fake, fake, None, fake, fake, 128, 128, 128, None) == 1
         assert fn(fake, fake, fake, fake, fake, 128, 256, 0, None) == 2
+        assert fn(fake, fake, fake, fake, fake, 0, 256, 128, None) == 2     # no tokens
+        assert fn(fake, fake, fake, fake, fake, -5, 256, 128, None) == 2
         assert fn(fake, fake, fake, fake, fake, 128, 200, 128, None) == 2
         assert fn(fake, fake, fake, odd, fake, 128, 128, 128, None) == 3
     assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, None, None) == 1
@@ -80,7 +83,8 @@ def test_validation_before_launch(lib):
     assert lib.fp8bs_set_workspace(fake, -1) == 1
     assert lib.fp8bs_set_workspace(fake, 1000) == 1               # below the 64 KiB flag region
     assert lib.fp8bs_set_workspace(ctypes.c_void_p(0x10010), 1 << 20) == 3
-    assert lib.fp8bs_gemm_wgrad_workspace_bytes(100, 128, 128) == -2
+    assert lib.fp8bs_gemm_wgrad_workspace_bytes(0, 128, 128) == -2
+    assert lib.fp8bs_gemm_wgrad_workspace_bytes(100, 100, 128) == -2
     assert lib.fp8bs_gemm_wgrad_workspace_bytes(128, 0, 128) == -2
 
 

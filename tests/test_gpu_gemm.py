@@ -94,6 +94,21 @@ def test_small_shapes_full_outputs(M, N, K):
     check_linear(x, w, dy, ("fprop", "dgrad", "wgrad"), seed)
 
 
+@pytest.mark.parametrize("M", [1, 100, 300])
+def test_token_counts_not_a_multiple_of_128(M):
+    """Token tails: the last 128-row tile of fprop/dgrad is partial, the last
+    128x1 token tile of the weight gradient's operands covers M % 128 tokens
+    (padding tokens are zeros).  Every quantized byte and scale (padding
+    included) and every GEMM output against the oracle."""
+    N, K = 384, 256
+    seed = 900 + M
+    x = inputs.random_bf16((M, K), seed=seed)
+    x[:, 7] *= 25.0
+    w = inputs.random_bf16((N, K), seed=seed + 1, std=0.02)
+    dy = inputs.random_bf16((M, N), seed=seed + 2, std=1e-3)
+    check_linear(x, w, dy, ("fprop", "dgrad", "wgrad"), seed)
+
+
 def test_persistent_tail_more_tiles_than_sms():
     # 148 SMs: 40 x 9 = 360 tiles of 128x256 -> every CTA loops, last wave partial.
     M, N, K = 5120, 2304, 256
@@ -241,7 +256,8 @@ def test_rejects_bad_arguments():
     t = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     p = t.data_ptr()
     assert lib.fp8bs_gemm_fprop(None, p, p, p, p, 128, 128, 128, None) == 1
-    assert lib.fp8bs_gemm_fprop(p, p, p, p, p, 100, 128, 128, None) == 2
+    assert lib.fp8bs_gemm_fprop(p, p, p, p, p, 128, 100, 128, None) == 2
+    assert lib.fp8bs_gemm_fprop(p, p, p, p, p, 0, 128, 128, None) == 2
     assert lib.fp8bs_gemm_wgrad(p, p, p, p, p, 128, 0, 128, None) == 2
     assert lib.fp8bs_gemm_dgrad(p + 8, p, p, p, p, 128, 128, 128, None) == 3
 

@@ -99,6 +99,17 @@ def test_colwise_and_fused_small_shapes_and_edge_tiles():
     check_colwise(x, fused=True)
 
 
+@pytest.mark.parametrize("rows", [1, 100, 129, 300])
+def test_token_tails_bit_exact(rows):
+    """Token counts that are not a multiple of 128, both layouts fused and
+    alone: payloads and scales (with the padding) equal the oracle's."""
+    x = inputs.random_bf16((rows, 384), seed=500 + rows)
+    x[:, 11] *= 45.0
+    check_rowwise(x)
+    check_colwise(x, fused=False)
+    check_colwise(x, fused=True)
+
+
 def test_weight_small_shapes_and_edge_blocks():
     w = inputs.random_bf16((384, 640), seed=103, std=0.02)
     w[:128, :128] = 0.0
