@@ -10,35 +10,44 @@
 // follow prescribes (blog section "FP8：加快 RTX 5090 上的训练"; arXiv part
 // 1/7, section 2.1).
 //
-// Persistent kernel, one 384-thread CTA per SM, 128 x BN output tiles
-// (BN = 256), K block 128:
-//   warp 0 (one lane): TMA producer -- A tile 128x128 B and B tile BNx128 B
-//       per K block into a shared-memory ring (128-byte swizzle);
-//   warp 1 (one lane): MMA issuer -- four tcgen05.mma (K = 32 each) per K
-//       block into one of two 128 x BN FP32 TMEM buffers (all 512 columns),
-//       the first with accumulate off, then commits to free the smem stage
-//       and to publish the buffer;
+// Persistent kernel, one 384-thread CTA per SM, 128 x 256 output tiles, K
+// block 128; the warps' loops run converged and one lane issues the TMA and
+// tcgen05 instructions:
+//   warp 0: TMA producer -- A tile 128x128 B and B tile 256x128 B per K block
+//       into a 3-stage shared-memory ring (128-byte swizzle);
+//   warp 1: MMA issuer -- four tcgen05.mma (K = 32 each) per K block into one
+//       of two 128 x 256 FP32 TMEM buffers (all 512 columns), the first with
+//       accumulate off, then commits to free the smem stage and to publish
+//       the buffer;
 //   warp 2: scale loader -- per K block the 128 row scales (and, for the
-//       weight gradient, the BN column scales) into an 8-slot shared-memory
+//       weight gradient, the 256 column scales) into an 8-slot shared-memory
 //       ring with cp.async, one 16-byte copy per lane;
 //   warp 3: idle (it completes the first warpgroup, whose registers are
 //       handed to the epilogue warpgroups with setmaxnreg);
 //   warps 4..11: promotion + epilogue -- each warp owns a 32-lane TMEM
-//       quadrant (rows) and one BN/2-column half; per K block it loads its
+//       quadrant (rows) and one 128-column half; per K block it loads its
 //       partial with tcgen05.ld two 32-column chunks at a time, releases the
 //       TMEM buffer after the last load, and does acc = fma(P_b, sa*sb, acc)
-//       with packed FP32 FMAs on BN/2 registers per thread; at the end of a
-//       tile it rounds to BF16 and stores.
+//       with packed FP32 FMAs on 128 registers per thread; at the end of a
+//       tile it writes the result through swizzled shared staging and TMA
+//       (BF16 stores, or FP32 reduce-adds for an accumulating weight
+//       gradient).
 // While the epilogue promotes block b, the tensor cores already compute
 // block b+1 into the other buffer.
+//
+// Work comes in units (tile, K range): one per tile, or, for a weight
+// gradient with few tiles, 2-4 splits of the token contraction whose FP32
+// partials meet in caller-provided scratch (see Params::splits).  Rows past
+// the output's last row (a token count that is not a multiple of 128) read
+// zeros through TMA and are not stored.
 //
 // The scale ring is written with cp.async (generic proxy) rather than TMA:
 // the epilogue reads it with ordinary loads, and a TMA write into a slot
 // those loads have just released would need a proxy fence per K block.
 //
-// Every mbarrier wait is bounded (see WaitCtx): on expiry the CTA records
-// a timeout in the device status word, waits (bounded) for its own copies
-// and MMAs in flight, frees its TMEM and returns.
+// Every wait is bounded (see WaitCtx): on expiry the CTA records a timeout
+// in the device status word, waits (bounded) for its own copies and MMAs in
+// flight, frees its TMEM and returns.
 #pragma once
 
 #include <cstdint>
