@@ -26,7 +26,6 @@ import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -58,8 +57,29 @@ def load_peaks():
 
 # ------------------------------------------------------------------ clocks
 
+# Runs in its own interpreter, so the sampling keeps its pace while the
+# benchmark's launch loop holds the GIL.  Samples every 2 ms until a line
+# (or EOF) arrives on stdin, then prints them.
+_SAMPLER_SRC = r"""
+import select, sys, time
+import pynvml
+pynvml.nvmlInit()
+key = sys.argv[1]
+h = (pynvml.nvmlDeviceGetHandleByUUID(key) if key.startswith("GPU-")
+     else pynvml.nvmlDeviceGetHandleByIndex(int(key)))
+print("ready", pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM), flush=True)
+out = []
+while not select.select([sys.stdin], [], [], 0)[0]:
+    out.append("%d %d" % (pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM),
+                          pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)))
+    time.sleep(0.002)
+print("\n".join(out), flush=True)
+"""
+
+
 class ClockSampler:
-    """Samples SM clock and clock-event reasons every 5 ms while running."""
+    """Samples the SM clock and the clock-event reasons of one GPU (NVML,
+    every ~2 ms, in a child process) between start() and stop()."""
 
     REASONS = {
         "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
@@ -67,50 +87,43 @@ class ClockSampler:
         "hw_power_brake_slowdown": 0x80, "display_clock_setting": 0x100,
     }
 
-    def __init__(self, device_index: int):
-        self.idx = device_index
-        self.samples = []
+    def __init__(self, device: torch.device):
+        key = str(device.index if device.index is not None else 0)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        self.key = key
         self.max_mhz = None
-        self._stop = threading.Event()
-        self._thread = None
-        self._nvml = None
+        self.samples = []
+        self._proc = None
 
     def start(self):
         try:
-            import pynvml
-
-            pynvml.nvmlInit()
-            h = pynvml.nvmlDeviceGetHandleByIndex(self.idx)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-            self._nvml = (pynvml, h)
+            self._proc = subprocess.Popen([sys.executable, "-c", _SAMPLER_SRC, self.key], stdin=subprocess.PIPE,
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self._proc.stdout.readline().split()
+            if len(first) == 2 and first[0] == "ready":
+                self.max_mhz = int(first[1])
+            else:
+                self._proc.kill()
+                self._proc.wait()
+                self._proc = None
         except Exception:
-            self._nvml = None
-        self._thread = threading.Thread(target=self._run, daemon=True)
-        self._thread.start()
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                if self._nvml:
-                    pynvml, h = self._nvml
-                    mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
-                    reasons = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-                    self.samples.append((mhz, reasons))
-                else:
-                    out = subprocess.check_output(
-                        ["nvidia-smi", "-i", str(self.idx), "--query-gpu=clocks.sm,clocks.max.sm",
-                         "--format=csv,noheader,nounits"], text=True)
-                    a, b = [int(v) for v in out.strip().split(",")]
-                    self.max_mhz = b
-                    self.samples.append((a, 0))
-            except Exception:
-                pass
-            self._stop.wait(0.005)
+            self._proc = None
 
     def stop(self):
-        self._stop.set()
-        if self._thread:
-            self._thread.join()
+        if self._proc is not None:
+            try:
+                out, _ = self._proc.communicate("stop\n", timeout=30)
+                for line in out.splitlines():
+                    f = line.split()
+                    if len(f) == 2:
+                        self.samples.append((int(f[0]), int(f[1])))
+            except Exception:
+                self._proc.kill()
+                self._proc.wait()
         seen = 0
         for _, r in self.samples:
             seen |= r
@@ -389,7 +402,7 @@ def run_ours(args):
     count0 = B.fp8bs_launch_count()
     D.barrier(ranks, device)
     torch.cuda.synchronize()
-    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks = ClockSampler(device)
     clocks.start()
     total_ms, per = time_step(lls, args.steps, per_launch=True)
     clk = clocks.stop()
