@@ -57,80 +57,134 @@ def load_peaks():
 
 # ------------------------------------------------------------------ clocks
 
-# Runs in its own interpreter, so the sampling keeps its pace while the
-# benchmark's launch loop holds the GIL.  Samples every 2 ms until a line
-# (or EOF) arrives on stdin, then prints them.
+# Samplers run in their own process, so they keep their pace while the
+# benchmark's launch loop holds the GIL.  With NVML's Python binding: a child
+# interpreter samples every ~2 ms until a line (or EOF) arrives on stdin, then
+# prints its samples.  Without it: `nvidia-smi -lms`.
 _SAMPLER_SRC = r"""
 import select, sys, time
-import pynvml
-pynvml.nvmlInit()
-key = sys.argv[1]
-h = (pynvml.nvmlDeviceGetHandleByUUID(key) if key.startswith("GPU-")
-     else pynvml.nvmlDeviceGetHandleByIndex(int(key)))
-print("ready", pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM), flush=True)
+try:
+    import pynvml
+    pynvml.nvmlInit()
+    h = None
+    for key in sys.argv[1:]:
+        try:
+            h = (pynvml.nvmlDeviceGetHandleByUUID(key) if key.startswith("GPU-")
+                 else pynvml.nvmlDeviceGetHandleByIndex(int(key)))
+            break
+        except Exception:
+            pass
+    if h is None:
+        raise RuntimeError("no NVML handle for " + " or ".join(sys.argv[1:]))
+    print("ready", pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM), flush=True)
+except Exception as e:
+    print("error", repr(e).replace("\n", " "), flush=True)
+    sys.exit(0)
 out = []
 while not select.select([sys.stdin], [], [], 0)[0]:
-    out.append("%d %d" % (pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM),
-                          pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)))
+    out.append("%d %d %d" % (pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM),
+                             pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM),
+                             pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)))
     time.sleep(0.002)
 print("\n".join(out), flush=True)
 """
 
 
 class ClockSampler:
-    """Samples the SM clock and the clock-event reasons of one GPU (NVML,
-    every ~2 ms, in a child process) between start() and stop()."""
+    """Samples the SM clock and the clock-event reasons of one GPU between
+    start() and stop(), from a separate process (NVML, else nvidia-smi)."""
 
     REASONS = {
         "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
         "sync_boost": 0x10, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
         "hw_power_brake_slowdown": 0x80, "display_clock_setting": 0x100,
     }
+    SMI_QUERY = "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active"
 
     def __init__(self, device: torch.device):
-        key = str(device.index if device.index is not None else 0)
+        # The device's UUID names the right GPU under CUDA_VISIBLE_DEVICES;
+        # its index is the fallback.
+        self.keys = []
         try:
             uuid = str(torch.cuda.get_device_properties(device).uuid)
-            key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.keys.append(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
         except Exception:
             pass
-        self.key = key
-        self.max_mhz = None
-        self.samples = []
+        self.keys.append(str(device.index if device.index is not None else 0))
+        self.samples = []          # (sm MHz, max sm MHz, reasons bitmask)
+        self.source = None
+        self.error = None
         self._proc = None
 
     def start(self):
         try:
-            self._proc = subprocess.Popen([sys.executable, "-c", _SAMPLER_SRC, self.key], stdin=subprocess.PIPE,
-                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            first = self._proc.stdout.readline().split()
-            if len(first) == 2 and first[0] == "ready":
-                self.max_mhz = int(first[1])
-            else:
+            import importlib.util
+
+            have_nvml = importlib.util.find_spec("pynvml") is not None
+        except Exception:
+            have_nvml = False
+        try:
+            if have_nvml:
+                env = dict(os.environ)
+                env["PYTHONPATH"] = os.pathsep.join(p for p in sys.path if p)
+                self._proc = subprocess.Popen([sys.executable, "-c", _SAMPLER_SRC, *self.keys],
+                                              stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                                              stderr=subprocess.STDOUT, text=True, env=env)
+                first = self._proc.stdout.readline()
+                if first.startswith("ready"):
+                    self.source = "nvml"
+                    return
+                self.error = first.strip()[:200] or "NVML sampler exited"
                 self._proc.kill()
                 self._proc.wait()
-                self._proc = None
-        except Exception:
+            key = None
+            for k in self.keys:          # the first id nvidia-smi accepts
+                r = subprocess.run(["nvidia-smi", "-i", k, "--query-gpu=clocks.max.sm", "--format=csv,noheader"],
+                                   capture_output=True, text=True, timeout=60)
+                if r.returncode == 0:
+                    key = k
+                    break
+            if key is None:
+                raise RuntimeError("nvidia-smi accepts none of " + ", ".join(self.keys))
+            self._proc = subprocess.Popen(["nvidia-smi", "-i", key, self.SMI_QUERY,
+                                           "--format=csv,noheader,nounits", "-lms", "10"],
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
+        except Exception as e:
+            self.error = ((self.error + "; ") if self.error else "") + repr(e)[:200]
             self._proc = None
 
     def stop(self):
         if self._proc is not None:
             try:
-                out, _ = self._proc.communicate("stop\n", timeout=30)
-                for line in out.splitlines():
-                    f = line.split()
-                    if len(f) == 2:
-                        self.samples.append((int(f[0]), int(f[1])))
-            except Exception:
+                if self.source == "nvml":
+                    out, _ = self._proc.communicate("stop\n", timeout=30)
+                    for line in out.splitlines():
+                        f = line.split()
+                        if len(f) == 3:
+                            self.samples.append((int(f[0]), int(f[1]), int(f[2])))
+                else:
+                    self._proc.terminate()
+                    out, _ = self._proc.communicate(timeout=30)
+                    for line in out.splitlines():
+                        f = [v.strip() for v in line.split(",")]
+                        if len(f) == 3 and f[0].isdigit() and f[1].isdigit():
+                            self.samples.append((int(f[0]), int(f[1]), int(f[2], 16)))
+            except Exception as e:
+                self.error = ((self.error + "; ") if self.error else "") + repr(e)[:200]
                 self._proc.kill()
                 self._proc.wait()
         seen = 0
-        for _, r in self.samples:
+        for _, _, r in self.samples:
             seen |= r
         names = sorted(n for n, bit in self.REASONS.items() if seen & bit)
-        mhz = [m for m, _ in self.samples]
-        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
-                "reasons": names, "samples": len(mhz)}
+        mhz = [m for m, _, _ in self.samples]
+        out = {"sm_mhz": statistics.median(mhz) if mhz else None,
+               "sm_max_mhz": max(x for _, x, _ in self.samples) if self.samples else None,
+               "reasons": names, "samples": len(mhz), "source": self.source}
+        if self.error:
+            out["error"] = self.error
+        return out
 
 
 # ------------------------------------------------------------------ our arm
@@ -540,7 +594,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=150)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
