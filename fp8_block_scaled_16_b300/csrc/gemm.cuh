@@ -83,7 +83,13 @@ struct Tile {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = 3;
     static constexpr int SA_FLOATS = BM;
-    static constexpr int SB_FLOATS = BN;
+    // Weight-gradient column scales, regrouped for the promotion threads: per
+    // 128-column half, four groups (one per t%4 of a .16x256b load) of the 32
+    // columns such a thread holds, each group padded to 36 floats so that the
+    // four groups start in different banks.
+    static constexpr int SB_GROUP = 36;
+    static constexpr int SB_HALF = 4 * SB_GROUP;
+    static constexpr int SB_FLOATS = 2 * SB_HALF;
     static constexpr int SLOT_FLOATS = SA_FLOATS + SB_FLOATS;
     static constexpr int COLS = BN / 2;                           // columns per epilogue warp
     static constexpr int OFF_A = 0;
@@ -100,6 +106,7 @@ struct Tile {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment for 128-byte swizzle");
     static_assert(COLS == 128, "epilogue chunking assumes 128 columns per warp");
+    static_assert(SB_FLOATS >= BN && (SA_FLOATS + SB_FLOATS) % 4 == 0, "scale slot layout");
     static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
     // barrier indices
     static __device__ __forceinline__ uint32_t full(int s) { return s; }
@@ -200,6 +207,13 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// 4- and 8-byte forms (cached at all levels; the only variant with these sizes).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
@@ -221,35 +235,36 @@ __device__ __forceinline__ void promote_scalar(float (&acc)[N], int base, const 
     }
 }
 
-// Rank-1 block scale (weight gradient): the FP32 product sa * sb[j] is
-// rounded first, then fused into the accumulator, as for a scalar scale.
+// Weight gradient, .16x256b layout: `lo` holds lanes 0-15 and `hi` lanes 16-31
+// of the warp's quadrant for the same 64 columns; thread t's rows are
+// t/4, t/4+8 (lo) and t/4+16, t/4+24 (hi), with row scales sa4.x..w, and its
+// columns 8g + 2(t%4) + {0,1} (g = 0..7), whose scales are cs[2g], cs[2g+1].
+// The FP32 product of row and column scale is rounded first, then fused into
+// the accumulator, as for a scalar scale.
 template <int N>
-__device__ __forceinline__ void promote_vector(float (&acc)[N], int base, const uint32_t (&r)[32], float sa,
-                                               const float* sbv) {
-    const float2 sa2 = make_float2(sa, sa);
+__device__ __forceinline__ void promote_rank1(float (&acc)[N], int base_lo, int base_hi, const uint32_t (&lo)[32],
+                                              const uint32_t (&hi)[32], float4 sa4, const float* cs) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sbv + base + i);
-        const float2 c0 = __fmul2_rn(sa2, make_float2(s4.x, s4.y));
-        const float2 c1 = __fmul2_rn(sa2, make_float2(s4.z, s4.w));
-        const float2 d0 = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c0,
-                                     make_float2(acc[base + i], acc[base + i + 1]));
-        const float2 d1 = __ffma2_rn(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), c1,
-                                     make_float2(acc[base + i + 2], acc[base + i + 3]));
-        acc[base + i] = d0.x;
-        acc[base + i + 1] = d0.y;
-        acc[base + i + 2] = d1.x;
-        acc[base + i + 3] = d1.y;
+    for (int gp = 0; gp < 4; gp++) {
+        const float4 c4 = *reinterpret_cast<const float4*>(cs + 4 * gp);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; h2++) {
+            const int g = 2 * gp + h2;
+            const float2 c2 = h2 ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+            const float sr[4] = {sa4.x, sa4.y, sa4.z, sa4.w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t(&r)[32] = q < 2 ? lo : hi;
+                const int i = 4 * g + 2 * (q & 1);
+                const int a = (q < 2 ? base_lo : base_hi) + i;
+                const float2 sc = __fmul2_rn(make_float2(sr[q], sr[q]), c2);
+                const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sc,
+                                            make_float2(acc[a], acc[a + 1]));
+                acc[a] = d.x;
+                acc[a + 1] = d.y;
+            }
+        }
     }
-}
-
-template <int SBMODE, int N>
-__device__ __forceinline__ void promote(float (&acc)[N], int base, const uint32_t (&r)[32], float sa, float sc,
-                                        const float* sbv) {
-    if constexpr (SBMODE == SB_SCALAR)
-        promote_scalar(acc, base, r, sc);
-    else
-        promote_vector(acc, base, r, sa, sbv);
 }
 
 template <int SBMODE, int BN>
@@ -389,16 +404,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::sempty(slot)), sph ^ 1u, wc)) { ok = false; break; }
                 const uint32_t dst = ring + static_cast<uint32_t>(slot * T::SLOT_FLOATS * 4);
-                cp_async_16(dst + lane * 16, p.sa + static_cast<int64_t>(kb) * p.sa_ld + mb * BM + lane * 4);
-                if constexpr (SBMODE == SB_VECTOR) {
+                const float* sa_src = p.sa + static_cast<int64_t>(kb) * p.sa_ld + mb * BM;
+                if constexpr (SBMODE == SB_SCALAR) {
+                    cp_async_16(dst + lane * 16, sa_src + lane * 4);
+                } else {
 #pragma unroll
-                    for (int c = 0; c < BN / 128; c++) {
-                        // Columns past the output's end (a ragged last tile) copy any valid
-                        // scale: those columns are computed but never stored.
-                        int64_t col = static_cast<int64_t>(nb) * BN + c * 128 + lane * 4;
-                        if (col >= p.cols) col = 0;
-                        cp_async_16(dst + (T::SA_FLOATS + c * 128) * 4 + lane * 16,
-                                    p.sb + static_cast<int64_t>(kb) * p.cols + col);
+                    for (int i = 0; i < 4; i++) {
+                        // Row 32q + 8i' + u goes to 32q + 4u + i': the four rows a
+                        // promotion thread holds (u = t/4) form one float4.
+                        const int row = lane * 4 + i;
+                        const int pos = (row & ~31) + 4 * (row & 7) + ((row >> 3) & 3);
+                        cp_async_4(dst + pos * 4, sa_src + row);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        // Column pair 2pr, 2pr+1 = h*128 + 64m + 8g + 2c + {0,1} goes to
+                        // group (h, c) at 16m + 2g.  Columns past the output's end (a
+                        // ragged last tile) copy any valid scale: they are never stored.
+                        const int col = 2 * (lane * 4 + i);
+                        const int h = col >> 7, w = col & 127;
+                        const int pos = T::SA_FLOATS + h * T::SB_HALF + ((w >> 1) & 3) * T::SB_GROUP +
+                                        16 * (w >> 6) + 2 * ((w >> 3) & 7);
+                        int64_t gcol = static_cast<int64_t>(nb) * BN + col;
+                        if (gcol >= p.cols) gcol = 0;
+                        cp_async_8(dst + pos * 4, p.sb + static_cast<int64_t>(kb) * p.cols + gcol);
                     }
                 }
                 cp_async_arrive(bar(T::sfull(slot)));
@@ -435,37 +464,59 @@ __global__ void __launch_bounds__(THREADS, 1)
                     sb_next = __ldg(p.sb + jb * p.sb_stride_j + (kb + 1) * p.sb_stride_b);
                 if (!warp_wait_bounded(bar(T::sfull(slot)), sph, wc)) { ok = false; break; }
                 const float* sl = ring + slot * T::SLOT_FLOATS;
-                const float sa = sl[row];
-                const float sc = __fmul_rn(sa, sb_cur);
-                const float* sbv = sl + T::SA_FLOATS + half * COLS;
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
+                                       static_cast<uint32_t>(tb * BN + half * COLS);
+                uint32_t ra[32], rb[32];
                 if constexpr (SBMODE == SB_SCALAR) {
+                    // Accumulator slice in the .32x32b layout: thread = row, register =
+                    // column; one scale per thread per K block.
+                    const float sc = __fmul_rn(sl[row], sb_cur);
                     // Only the row scale is needed from the slot: free it now.
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(T::sempty(slot)));
-                }
-                if (!warp_wait_bounded(bar(T::tfull(tb)), tph, wc)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       static_cast<uint32_t>(tb * BN + half * COLS);
-                // Two 32-column chunks in flight per wait; the TMEM buffer is
-                // released as soon as the last chunk is in registers.
-                uint32_t ra[32], rb[32];
-                tmem_ld_32cols(taddr + 0, ra);
-                tmem_ld_32cols(taddr + 32, rb);
-                tmem_wait_ld(ra);
-                reg_fence(rb);
-                promote<SBMODE>(acc, 0, ra, sa, sc, sbv);
-                promote<SBMODE>(acc, 32, rb, sa, sc, sbv);
-                tmem_ld_32cols(taddr + 64, ra);
-                tmem_ld_32cols(taddr + 96, rb);
-                tmem_wait_ld(ra);
-                reg_fence(rb);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(T::tempty(tb)));
-                promote<SBMODE>(acc, 64, ra, sa, sc, sbv);
-                promote<SBMODE>(acc, 96, rb, sa, sc, sbv);
-                if constexpr (SBMODE == SB_VECTOR) {
+                    if (!warp_wait_bounded(bar(T::tfull(tb)), tph, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    // Two 32-column chunks in flight per wait; the TMEM buffer is
+                    // released as soon as the last chunk is in registers.
+                    tmem_ld_32cols(taddr + 0, ra);
+                    tmem_ld_32cols(taddr + 32, rb);
+                    tmem_wait_ld(ra);
+                    reg_fence(rb);
+                    promote_scalar(acc, 0, ra, sc);
+                    promote_scalar(acc, 32, rb, sc);
+                    tmem_ld_32cols(taddr + 64, ra);
+                    tmem_ld_32cols(taddr + 96, rb);
+                    tmem_wait_ld(ra);
+                    reg_fence(rb);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::tempty(tb)));
+                    promote_scalar(acc, 64, ra, sc);
+                    promote_scalar(acc, 96, rb, sc);
+                } else {
+                    // Weight gradient: the scale is row scale x column scale, so the slice
+                    // is read in the .16x256b layout (4 rows x 32 columns per thread), which
+                    // needs 8 shared-memory loads of column scales per K block instead of
+                    // 32 with one row per thread.  acc[32L + i]: L = 0,1 lanes 0-15 and
+                    // L = 2,3 lanes 16-31 of the quadrant; L even columns 0-63, odd 64-127.
+                    const float4 sa4 = *reinterpret_cast<const float4*>(sl + quad * 32 + 4 * (lane >> 2));
+                    const float* cs = sl + T::SA_FLOATS + half * T::SB_HALF + (lane & 3) * T::SB_GROUP;
+                    if (!warp_wait_bounded(bar(T::tfull(tb)), tph, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t thi = taddr + (16u << 16);
+                    tmem_ld_16x256b_x8(taddr, ra);
+                    tmem_ld_16x256b_x8(thi, rb);
+                    tmem_wait_ld(ra);
+                    reg_fence(rb);
+                    promote_rank1(acc, 0, 64, ra, rb, sa4, cs);
+                    tmem_ld_16x256b_x8(taddr + 64, ra);
+                    tmem_ld_16x256b_x8(thi + 64, rb);
+                    tmem_wait_ld(ra);
+                    reg_fence(rb);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::tempty(tb)));
+                    promote_rank1(acc, 32, 96, ra, rb, sa4, cs + 16);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(T::sempty(slot)));
                 }
@@ -521,16 +572,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int h = 0; h < 2; h++) {
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
+                    if constexpr (SBMODE == SB_SCALAR) {
 #pragma unroll
-                    for (int b = 0; b < 2; b++) {
+                        for (int b = 0; b < 2; b++) {
 #pragma unroll
-                        for (int c = 0; c < 8; c++) {
-                            const int j = h * 64 + b * 32 + c * 4;
-                            const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
-                                                                                 ((c ^ (lane & 7)) << 4));
-                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(acc[j]),
-                                         "f"(acc[j + 1]), "f"(acc[j + 2]), "f"(acc[j + 3])
-                                         : "memory");
+                            for (int c = 0; c < 8; c++) {
+                                const int j = h * 64 + b * 32 + c * 4;
+                                const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
+                                                                                     ((c ^ (lane & 7)) << 4));
+                                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(acc[j]),
+                                             "f"(acc[j + 1]), "f"(acc[j + 2]), "f"(acc[j + 3])
+                                             : "memory");
+                            }
+                        }
+                    } else {
+                        // .16x256b layout: columns 64h + 8g + 2(t%4) + {0,1} of rows
+                        // 16Lh + t/4 + 8hi come from acc[32(h + 2Lh) + 4g + 2hi].
+                        const int u = lane >> 2, c = lane & 3;
+#pragma unroll
+                        for (int lh = 0; lh < 2; lh++) {
+#pragma unroll
+                            for (int g = 0; g < 8; g++) {
+#pragma unroll
+                                for (int hi = 0; hi < 2; hi++) {
+                                    const int j = 32 * (h + 2 * lh) + 4 * g + 2 * hi;
+                                    const int rr = 16 * lh + 8 * hi + u;
+                                    const int chunk = 2 * (g & 3) + (c >> 1);
+                                    const uint32_t a = stage_out + static_cast<uint32_t>((g >> 2) * T::OUT_BOX_BYTES +
+                                                                                         rr * 128 + ((chunk ^ u) << 4) +
+                                                                                         8 * (c & 1));
+                                    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(acc[j]), "f"(acc[j + 1])
+                                                 : "memory");
+                                }
+                            }
                         }
                     }
                     fence_proxy_async_smem();
@@ -550,20 +624,42 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
                 if (lane == 0) bulk_wait_read_all();  // the previous tile's stores have read the buffer
                 __syncwarp();
+                if constexpr (SBMODE == SB_SCALAR) {
 #pragma unroll
-                for (int b = 0; b < 2; b++) {
+                    for (int b = 0; b < 2; b++) {
 #pragma unroll
-                    for (int c = 0; c < 8; c++) {
-                        const int j = b * 64 + c * 8;
-                        const uint32_t w0 = f32x2_to_bf16x2(acc[j + 0], acc[j + 1]);
-                        const uint32_t w1 = f32x2_to_bf16x2(acc[j + 2], acc[j + 3]);
-                        const uint32_t w2 = f32x2_to_bf16x2(acc[j + 4], acc[j + 5]);
-                        const uint32_t w3 = f32x2_to_bf16x2(acc[j + 6], acc[j + 7]);
-                        const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
-                                                                             ((c ^ (lane & 7)) << 4));
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1),
-                                     "r"(w2), "r"(w3)
-                                     : "memory");
+                        for (int c = 0; c < 8; c++) {
+                            const int j = b * 64 + c * 8;
+                            const uint32_t w0 = f32x2_to_bf16x2(acc[j + 0], acc[j + 1]);
+                            const uint32_t w1 = f32x2_to_bf16x2(acc[j + 2], acc[j + 3]);
+                            const uint32_t w2 = f32x2_to_bf16x2(acc[j + 4], acc[j + 5]);
+                            const uint32_t w3 = f32x2_to_bf16x2(acc[j + 6], acc[j + 7]);
+                            const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
+                                                                                 ((c ^ (lane & 7)) << 4));
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1),
+                                         "r"(w2), "r"(w3)
+                                         : "memory");
+                        }
+                    }
+                } else {
+                    // .16x256b layout: acc[32L + 4g + 2hi], {+1} is row 16(L/2) + 8hi + t/4,
+                    // columns 64(L%2) + 8g + 2(t%4) + {0,1}: one BF16 pair per store, the
+                    // eight rows of a store in eight different 16-byte chunks.
+                    const int u = lane >> 2, c = lane & 3;
+#pragma unroll
+                    for (int L = 0; L < 4; L++) {
+#pragma unroll
+                        for (int g = 0; g < 8; g++) {
+#pragma unroll
+                            for (int hi = 0; hi < 2; hi++) {
+                                const int j = 32 * L + 4 * g + 2 * hi;
+                                const int rr = 16 * (L >> 1) + 8 * hi + u;
+                                const uint32_t a = stage_out + static_cast<uint32_t>((L & 1) * T::OUT_BOX_BYTES +
+                                                                                     rr * 128 + ((g ^ u) << 4) + 4 * c);
+                                asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(f32x2_to_bf16x2(acc[j], acc[j + 1]))
+                                             : "memory");
+                            }
+                        }
                     }
                 }
                 fence_proxy_async_smem();
