@@ -21,6 +21,7 @@ from . import build as _build
 
 ROWWISE = 1
 COLWISE_T = 2
+OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2   # fp8bs_gemm_workspace_bytes products
 
 STATUS = {
     0: "FP8BS_OK", 1: "FP8BS_ERR_INVALID_ARG", 2: "FP8BS_ERR_SHAPE", 3: "FP8BS_ERR_ALIGN",
@@ -38,6 +39,8 @@ SIGNATURES = {
     "fp8bs_gemm_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_get_device_status": (ctypes.c_int, [_P]),
     "fp8bs_set_workspace": (ctypes.c_int, [_P, _I64]),
+    "fp8bs_gemm_workspace_bytes": (_I64, [ctypes.c_int, _I64, _I64, _I64]),
+    "fp8bs_debug_split_plan": (ctypes.c_int, [_I64, _I64, ctypes.c_int, _P]),
     "fp8bs_gemm_wgrad_workspace_bytes": (_I64, [_I64, _I64, _I64]),
     "fp8bs_gemm_wgrad_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_gemm_wgrad_accumulate_f32": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -160,10 +163,13 @@ def fp8bs_quantize_weight(w: torch.Tensor, q=None, qT=None, s=None, want_t: bool
     return q, qT, s
 
 
-def fp8bs_gemm_fprop(xq, sx, wq, sw, y=None, stream=None) -> torch.Tensor:
-    """Y [M][N] BF16 = X W^T from Xq [M][K], sx [K/128][Mp], Wq [N][K], sw [N/128][K/128]."""
+def fp8bs_gemm_fprop(xq, sx, wq, sw, y=None, stream=None, split=True) -> torch.Tensor:
+    """Y [M][N] BF16 = X W^T from Xq [M][K], sx [K/128][Mp], Wq [N][K], sw [N/128][K/128].
+    With split=True the binding makes sure split-K scratch is registered."""
     M, K = xq.shape
     N = wq.shape[0]
+    if split:
+        _ensure_workspace(OP_FPROP, M, N, K, xq.device)
     y = _out(y, (M, N), torch.bfloat16, xq.device)
     _check(load().fp8bs_gemm_fprop(
         _dev(xq, torch.uint8, (M, K), "xq"), _dev(sx, torch.float32, (K // 128, padded_tokens(M)), "sx"),
@@ -172,10 +178,13 @@ def fp8bs_gemm_fprop(xq, sx, wq, sw, y=None, stream=None) -> torch.Tensor:
     return y
 
 
-def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None) -> torch.Tensor:
-    """dX [M][K] BF16 = dY W from dYq [M][N], sdy [N/128][Mp], WqT [K][N], sw [N/128][K/128]."""
+def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None, split=True) -> torch.Tensor:
+    """dX [M][K] BF16 = dY W from dYq [M][N], sdy [N/128][Mp], WqT [K][N], sw [N/128][K/128].
+    With split=True the binding makes sure split-K scratch is registered."""
     M, N = dyq.shape
     K = wqT.shape[0]
+    if split:
+        _ensure_workspace(OP_DGRAD, M, N, K, dyq.device)
     dx = _out(dx, (M, K), torch.bfloat16, dyq.device)
     _check(load().fp8bs_gemm_dgrad(
         _dev(dyq, torch.uint8, (M, N), "dyq"), _dev(sdy, torch.float32, (N // 128, padded_tokens(M)), "sdy"),
@@ -187,11 +196,11 @@ def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None) -> torch.Tensor:
 _workspaces = {}  # device index -> registered scratch tensor
 
 
-def _ensure_workspace(M: int, N: int, K: int, device) -> None:
-    """Registers (torch-allocated) scratch for the weight gradient's split-K
-    path if this shape would use more than the device has registered.  A
+def _ensure_workspace(op: int, M: int, N: int, K: int, device) -> None:
+    """Registers (torch-allocated) scratch for the split-K path of product
+    `op` if this shape would use more than the device has registered.  A
     new buffer replaces the old one only after the device is idle."""
-    need = int(load().fp8bs_gemm_wgrad_workspace_bytes(M, N, K))
+    need = int(load().fp8bs_gemm_workspace_bytes(op, M, N, K))
     if need <= 0:
         return
     idx = device.index if device.index is not None else torch.cuda.current_device()
@@ -217,6 +226,10 @@ def fp8bs_set_workspace(ws: Optional[torch.Tensor]) -> None:
     _workspaces[ws.device.index] = ws
 
 
+def fp8bs_gemm_workspace_bytes(op: int, M: int, N: int, K: int) -> int:
+    return int(load().fp8bs_gemm_workspace_bytes(op, M, N, K))
+
+
 def fp8bs_gemm_wgrad_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().fp8bs_gemm_wgrad_workspace_bytes(M, N, K))
 
@@ -228,7 +241,7 @@ def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None, split=True) -> 
     N, M = dyTq.shape
     K = xTq.shape[0]
     if split:
-        _ensure_workspace(M, N, K, dyTq.device)
+        _ensure_workspace(OP_WGRAD, M, N, K, dyTq.device)
     dw = _out(dw, (N, K), torch.bfloat16, dyTq.device)
     _check(load().fp8bs_gemm_wgrad(
         _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
@@ -241,7 +254,7 @@ def fp8bs_gemm_wgrad_accumulate_f32(dyTq, sdyT, xTq, sxT, dw, stream=None) -> to
     """dW (FP32 [N][K], updated in place) += dY^T X."""
     N, M = dyTq.shape
     K = xTq.shape[0]
-    _ensure_workspace(M, N, K, dyTq.device)
+    _ensure_workspace(OP_WGRAD, M, N, K, dyTq.device)
     _check(load().fp8bs_gemm_wgrad_accumulate_f32(
         _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
         _dev(xTq, torch.uint8, (K, M), "xTq"), _dev(sxT, torch.float32, (M // 128, K), "sxT"),
@@ -288,3 +301,12 @@ def fp8bs_debug_e4m3_encode_bits(first: int, n: int, out: Optional[torch.Tensor]
     _check(load().fp8bs_debug_e4m3_encode_bits(first, n, _dev(out, torch.uint8, (n,), "out"), _stream(stream)),
            "fp8bs_debug_e4m3_encode_bits")
     return out
+
+
+def fp8bs_debug_split_plan(tiles: int, kblocks: int, sms: int) -> dict:
+    """The library's split-K plan for a product of `tiles` output tiles and
+    `kblocks` contraction blocks on `sms` SMs (host computation only)."""
+    out = (ctypes.c_int64 * 4)()
+    _check(load().fp8bs_debug_split_plan(tiles, kblocks, sms, ctypes.cast(out, ctypes.c_void_p)),
+           "fp8bs_debug_split_plan")
+    return {"splits": out[0], "tail_first": out[1], "units": out[2], "bytes": out[3]}

@@ -41,7 +41,7 @@ struct DeviceInfo {
     int sm_count = 0;
     uint32_t* status = nullptr;
     bool gemm_attr_set[2] = {false, false};
-    // Caller-registered scratch for split-K weight gradients (fp8bs_set_workspace).
+    // Caller-registered scratch for split-K GEMMs (fp8bs_set_workspace).
     uint8_t* ws = nullptr;
     int64_t ws_bytes = 0;
     std::atomic<uint32_t> epoch{0};
@@ -129,30 +129,53 @@ int launch_status() {
     return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
-// Split-K plan for a weight gradient: the number of K splits per output tile
-// that fills the last wave of a persistent launch noticeably better (at
-// least 5 points of SM occupancy) than fewer splits, with at least 16 K
-// blocks per split and the split flags within the fixed flag region.
+// Split-K plan: K splits of some output tiles so that the persistent
+// launch's last wave is better filled.  Two forms:
+//   uniform: every tile in S parts (S = 2..4, at least 16 K blocks each);
+//   tail:    the tiles past the last full wave in S parts (S x tail tiles
+//            <= SMs, at least 4 K blocks each), the full waves whole.
+// Plans are compared by estimated time in K-block units (~0.6 us each): a
+// unit adds one block for its set-up and store; a helper's publication of
+// its 128 KB FP32 partial costs ~5 blocks and the owner's read-and-add ~2
+// blocks per partial (both limited by one SM's ~100 GB/s to L2, measured
+// on B300).  A plan is used only if it saves at least 5% over no split, and
+// only while its completion flags fit the fixed flag region.  So short
+// contractions (a forward product with K = 2048) are never split: moving
+// the partials would cost more than the idle SMs of the last wave.
 constexpr int64_t kFlagBytes = 64 * 1024;         // flag region at the start of the scratch
 constexpr int64_t kPartialBytes = 128 * 256 * 4;  // one tile's FP32 partial
 struct SplitPlan {
     int splits;
-    int64_t bytes;  // scratch needed (0 without splitting)
+    int64_t tail_first;  // tiles [0, tail_first) are not split
+    int64_t units;
+    int64_t bytes;       // scratch needed (0 without splitting)
 };
 SplitPlan plan_splits(int64_t tiles, int64_t kblocks, int sms) {
-    auto eff = [&](int64_t units) {
-        const int64_t waves = (units + sms - 1) / sms;
-        return static_cast<double>(units) / static_cast<double>(waves * sms);
+    auto waves = [&](int64_t units) { return static_cast<double>((units + sms - 1) / sms); };
+    constexpr double kUnitCost = 1.0, kPublishCost = 5.0, kAddCost = 2.0;
+    SplitPlan best{1, 0, tiles, 0};
+    const double t_none = waves(tiles) * (static_cast<double>(kblocks) + kUnitCost);
+    double best_t = t_none;
+    auto consider = [&](int s, int64_t first, double t) {
+        const int64_t split_tiles = tiles - first;
+        if ((s - 1) * split_tiles * gemm::NUM_EPI_WARPS * 4 > kFlagBytes) return;
+        if (t < best_t && t <= 0.95 * t_none) {
+            best = {s, first, first + s * split_tiles, kFlagBytes + (s - 1) * split_tiles * kPartialBytes};
+            best_t = t;
+        }
     };
-    SplitPlan best{1, 0};
-    double best_eff = eff(tiles);
-    for (int sp = 2; sp <= 4; sp++) {
-        if (kblocks % sp != 0 || kblocks / sp < 16) continue;
-        if ((sp - 1) * tiles * gemm::NUM_EPI_WARPS * 4 > kFlagBytes) continue;
-        const double e = eff(tiles * sp);
-        if (e > best_eff + 0.05) {
-            best = {sp, kFlagBytes + (sp - 1) * tiles * kPartialBytes};
-            best_eff = e;
+    for (int s = 2; s <= 4; s++) {
+        if (kblocks / s < 16) continue;
+        const double k = static_cast<double>((kblocks + s - 1) / s);
+        consider(s, 0, waves(tiles * s) * (k + kUnitCost) + kPublishCost + kAddCost * (s - 1));
+    }
+    const int64_t full = (tiles / sms) * sms, tail = tiles - full;
+    if (full > 0 && tail > 0) {
+        for (int s = 2; s <= 8; s++) {
+            if (s * tail > sms || kblocks / s < 4) continue;
+            const double k = static_cast<double>((kblocks + s - 1) / s);
+            consider(s, full, static_cast<double>(tiles / sms) * (static_cast<double>(kblocks) + kUnitCost) +
+                                  (k + kUnitCost) + kPublishCost + kAddCost * (s - 1));
         }
     }
     return best;
@@ -191,22 +214,25 @@ int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows,
     p.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
     p.fault = g_fault.exchange(0);
     p.splits = 1;
+    p.tail_first = 0;
     p.ws = nullptr;
     p.flags = nullptr;
     p.epoch = 0;
 
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
-    if (SBMODE == SB_VECTOR && d->ws != nullptr) {
+    int64_t units = tiles;
+    if (d->ws != nullptr) {
         const SplitPlan sp = plan_splits(tiles, p.kblocks, d->sm_count);
         if (sp.splits > 1 && sp.bytes <= d->ws_bytes) {
             p.splits = sp.splits;
+            p.tail_first = static_cast<int32_t>(sp.tail_first);
             p.flags = reinterpret_cast<uint32_t*>(d->ws);
             p.ws = reinterpret_cast<float*>(d->ws + kFlagBytes);
             p.epoch = d->epoch.fetch_add(1) + 1;
+            units = sp.units;
         }
     }
-    const int64_t units = tiles * p.splits;
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
 
     auto kern = gemm_kernel<SBMODE, BN>;
@@ -344,13 +370,25 @@ int fp8bs_set_workspace(void* ws, int64_t bytes) {
     return FP8BS_OK;
 }
 
-int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+int64_t fp8bs_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
     if (!tokens_ok(M) || !dim_ok(N) || !dim_ok(K)) return -FP8BS_ERR_SHAPE;
     DeviceInfo* d = nullptr;
     int rc = current_device(&d);
     if (rc != FP8BS_OK) return -rc;
-    const int64_t tiles = (N / gemm::BM) * ((K + 255) / 256);
-    return plan_splits(tiles, padded_tokens(M) / gemm::BK, d->sm_count).bytes;
+    // Output tiles (128 x 256) and contraction blocks of each product.
+    int64_t rows, cols, kc;
+    switch (op) {
+        case FP8BS_OP_FPROP: rows = M; cols = N; kc = K; break;
+        case FP8BS_OP_DGRAD: rows = M; cols = K; kc = N; break;
+        case FP8BS_OP_WGRAD: rows = N; cols = K; kc = padded_tokens(M); break;
+        default: return -FP8BS_ERR_INVALID_ARG;
+    }
+    const int64_t tiles = ((rows + gemm::BM - 1) / gemm::BM) * ((cols + 255) / 256);
+    return plan_splits(tiles, kc / gemm::BK, d->sm_count).bytes;
+}
+
+int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    return fp8bs_gemm_workspace_bytes(FP8BS_OP_WGRAD, M, N, K);
 }
 
 int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
@@ -409,13 +447,14 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
     p.fault = 0;
     p.out_f32_add = 0;
     p.splits = sp.splits;
+    p.tail_first = static_cast<int32_t>(sp.tail_first);
     p.ws = nullptr;
     p.flags = nullptr;
     p.epoch = 0;
     if (sp.splits > 1) {
         // The scratch keeps whatever the previous call left: clear the flags
         // this call will use (partials are always written before they are read).
-        const int64_t flag_bytes = (sp.splits - 1) * tiles * NUM_EPI_WARPS * 4;
+        const int64_t flag_bytes = (sp.splits - 1) * (tiles - sp.tail_first) * NUM_EPI_WARPS * 4;
         if (cudaMemsetAsync(d->noalloc_scratch, 0, static_cast<size_t>(flag_bytes), st) != cudaSuccess) {
             cudaGetLastError();
             return FP8BS_ERR_LAUNCH;
@@ -424,7 +463,7 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
         p.ws = reinterpret_cast<float*>(d->noalloc_scratch + kFlagBytes);
         p.epoch = 1;
     }
-    const int64_t units = tiles * p.splits;
+    const int64_t units = sp.units;
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
     auto kern = gemm_kernel<SB_VECTOR, 256>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
@@ -470,6 +509,18 @@ int64_t fp8bs_launch_count(void) { return g_launches.load(); }
 int fp8bs_debug_set_wait_timeout_ns(int64_t ns) {
     if (ns < 0) return FP8BS_ERR_INVALID_ARG;
     g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
+    return FP8BS_OK;
+}
+
+int fp8bs_debug_split_plan(int64_t tiles, int64_t kblocks, int sms, int64_t* out) {
+    using namespace fp8bs;
+    if (tiles <= 0 || kblocks <= 0 || sms <= 0 || out == nullptr || tiles > (int64_t(1) << 30))
+        return FP8BS_ERR_INVALID_ARG;
+    const SplitPlan sp = plan_splits(tiles, kblocks, sms);
+    out[0] = sp.splits;
+    out[1] = sp.tail_first;
+    out[2] = sp.units;
+    out[3] = sp.bytes;
     return FP8BS_OK;
 }
 

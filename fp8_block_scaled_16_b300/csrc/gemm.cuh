@@ -35,9 +35,10 @@
 // While the epilogue promotes block b, the tensor cores already compute
 // block b+1 into the other buffer.
 //
-// Work comes in units (tile, K range): one per tile, or, for a weight
-// gradient with few tiles, 2-4 splits of the token contraction whose FP32
-// partials meet in caller-provided scratch (see Params::splits).  Rows past
+// Work comes in units (tile, K range): one per tile, or, where the last wave
+// of tiles would leave many SMs idle, 2-8 splits of the contraction of some
+// or all tiles, whose FP32 partials meet in caller-provided scratch (see
+// Params::splits).  Rows past
 // the output's last row (a token count that is not a multiple of 128) read
 // zeros through TMA and are not stored.
 //
@@ -130,37 +131,53 @@ struct Params {
     uint32_t* status;
     uint64_t timeout_ns;
     int32_t fault;                // test hook: withhold CTA 0's first operand copy
-    // K splits per tile (weight gradient; 1 = none).  Split s > 0 of tile t is
-    // a helper that leaves its FP32 partial in ws slot (s-1)*tiles + t and
-    // sets flags[slot*8 + warp] = epoch; split 0 is the owner that adds the
-    // helpers' partials, in split order, before it stores the tile.
     int32_t out_f32_add;          // 0: BF16 store into out; 1: FP32 out += result (tmC is FP32)
+    // K splits (1 = none) of the tiles t >= tail_first (0: of every tile).
+    // With T = tiles - tail_first split tiles, split s > 0 of tile t is a
+    // helper that leaves its FP32 partial in ws slot (s-1)*T + (t-tail_first)
+    // and sets flags[slot*8 + warp] = epoch; split 0 is the owner that adds
+    // the helpers' partials, in split order, before it stores the tile.
     int32_t splits;
-    float* ws;                    // [(splits-1)*tiles][8 warps][32 float4][32 lanes]
-    uint32_t* flags;              // [(splits-1)*tiles][8]
+    int32_t tail_first;
+    float* ws;                    // [(splits-1)*T][8 warps][32 float4][32 lanes]
+    uint32_t* flags;              // [(splits-1)*T][8]
     uint32_t epoch;
 };
 
-// One unit of work: K blocks [kb0, kb1) of output tile t, split s.  Units
-// of every split s > 0 (helpers) are numbered before all owners (s == 0),
-// so a CTA, which takes its units in increasing order, has finished all of
-// its helper units before it can wait on anyone; helpers never wait.
+// One unit of work: K blocks [kb0, kb1) of output tile t, split s (split:
+// the tile is computed in parts).  Units are numbered whole tiles first
+// (t < tail_first), then the helpers (s > 0) of the split tiles, then their
+// owners (s == 0), so a CTA, which takes its units in increasing order, has
+// finished all of its whole-tile and helper units before it can wait on
+// anyone; those never wait.
 struct Unit {
     int t, s, kb0, kb1;
+    bool split;
 };
+__device__ __forceinline__ int num_units_of(const Params& p, int num_tiles) {
+    return p.tail_first + p.splits * (num_tiles - p.tail_first);
+}
 __device__ __forceinline__ Unit unit_of(int u, const Params& p, int num_tiles) {
     Unit w;
-    const int helpers = (p.splits - 1) * num_tiles;
-    if (u < helpers) {
-        w.s = 1 + u / num_tiles;
-        w.t = u - (w.s - 1) * num_tiles;
-    } else {
-        w.s = 0;
-        w.t = u - helpers;
+    w.s = 0;
+    w.split = false;
+    w.kb0 = 0;
+    w.kb1 = p.kblocks;
+    if (u < p.tail_first) {
+        w.t = u;
+        return w;
     }
-    const int per = p.kblocks / p.splits;
-    w.kb0 = w.s * per;
-    w.kb1 = w.kb0 + per;
+    const int v = u - p.tail_first, nt = num_tiles - p.tail_first;
+    const int helpers = (p.splits - 1) * nt;
+    if (v < helpers) {
+        w.s = 1 + v / nt;
+        w.t = p.tail_first + v - (w.s - 1) * nt;
+    } else {
+        w.t = p.tail_first + v - helpers;
+    }
+    w.split = p.splits > 1;
+    w.kb0 = static_cast<int>(static_cast<int64_t>(w.s) * p.kblocks / p.splits);
+    w.kb1 = static_cast<int>(static_cast<int64_t>(w.s + 1) * p.kblocks / p.splits);
     return w;
 }
 
@@ -314,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = misc[0];
     const WaitCtx wc{reinterpret_cast<volatile uint32_t*>(&misc[1]), p.status, p.timeout_ns};
     const int num_tiles = p.m_tiles * p.n_tiles;
-    const int num_units = num_tiles * p.splits;
+    const int num_units = num_units_of(p, num_tiles);
 
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
@@ -524,11 +541,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
             }
             if (!ok) break;
-            if constexpr (SBMODE == SB_VECTOR) {
+            if (w.split) {
+                const int nt = num_tiles - p.tail_first;
                 if (w.s > 0) {
                     // Helper: publish this warp's FP32 partial (lane-interleaved float4s,
                     // so every store instruction writes 512 contiguous bytes), then the flag.
-                    const int slot_id = (w.s - 1) * num_tiles + w.t;
+                    const int slot_id = (w.s - 1) * nt + (w.t - p.tail_first);
                     float4* dst = reinterpret_cast<float4*>(p.ws) + (static_cast<int64_t>(slot_id) * NUM_EPI_WARPS + ew) * 1024;
 #pragma unroll
                     for (int c = 0; c < 32; c++)
@@ -543,7 +561,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 // Owner: add the helpers' partials in split order.
                 for (int j = 1; ok && j < p.splits; j++) {
-                    const int slot_id = (j - 1) * num_tiles + w.t;
+                    const int slot_id = (j - 1) * nt + (w.t - p.tail_first);
                     const bool got = wait_flag(p.flags + slot_id * NUM_EPI_WARPS + ew, p.epoch, wc);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     const float4* src =

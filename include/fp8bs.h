@@ -162,29 +162,36 @@ int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, cons
                                     float* dw, int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
- * Scratch memory for the weight gradient's split-K path (caller-owned).
+ * Scratch memory for the GEMMs' split-K path (caller-owned).
  *
- * When a weight gradient has few output tiles (e.g. 2048 x 5632 outputs on
- * 148 SMs), fp8bs_gemm_wgrad splits the token contraction of each tile into
- * 2-4 parts computed by different CTAs; the parts' FP32 partial sums are
- * added in a fixed order (split 0 + split 1 + ...), so results stay
- * bitwise deterministic, and each part keeps the per-128-token promotion
- * chain.  The partial sums go through this scratch buffer:
+ * When the output tiles (128 x 256) of a product do not fill the last wave
+ * of the 148 SMs well and the contraction is long enough to pay for moving
+ * FP32 partial sums (a weight gradient over many tokens with few tiles, e.g.
+ * 2048 x 5632 outputs), the contraction of the last wave's tiles, or of all
+ * tiles, is split into 2-8 parts computed by different CTAs.  Each part
+ * keeps the per-128-K promotion chain; the parts' FP32 partial sums are
+ * added in a fixed order (part 0 + part 1 + ...), so results stay bitwise
+ * deterministic.  The partial sums go through this scratch buffer:
  *
- *   fp8bs_gemm_wgrad_workspace_bytes(M, N, K): bytes the current device
- *     needs for a weight gradient of that shape; 0 if it would not split;
- *     a negative status on bad shapes or no usable device.
+ *   fp8bs_gemm_workspace_bytes(op, M, N, K): bytes the current device needs
+ *     for product `op` (FP8BS_OP_FPROP, _DGRAD, _WGRAD) with the arguments
+ *     of that product's entry point; 0 if it would not split; a negative
+ *     status on bad shapes, an unknown op or no usable device.
+ *   fp8bs_gemm_wgrad_workspace_bytes(M, N, K): the same for FP8BS_OP_WGRAD.
  *   fp8bs_set_workspace(ws, bytes): registers `bytes` of DEVICE memory at
  *     `ws` (256-byte aligned, bytes >= 64 KiB; NULL and 0 unregister) as the
  *     current device's scratch.  The library zeroes its first 64 KiB (the
  *     completion flags) with a blocking cudaMemset and keeps the pointer; the
  *     caller keeps the memory alive and unmodified while it is registered,
- *     and registers only while no weight gradient is running.  Without a
- *     large enough registration the weight gradient simply does not split.
- *     Weight gradients that share one scratch must not overlap in time (two
- *     streams would race on it).
+ *     and registers only while no GEMM is running.  Without a large enough
+ *     registration a product simply does not split.  GEMMs that share one
+ *     scratch must not overlap in time (two streams would race on it).
  */
+#define FP8BS_OP_FPROP 0
+#define FP8BS_OP_DGRAD 1
+#define FP8BS_OP_WGRAD 2
 int fp8bs_set_workspace(void* ws, int64_t bytes);
+int64_t fp8bs_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -244,10 +251,16 @@ int64_t fp8bs_launch_count(void);
  *   fp8bs_debug_e4m3_encode_bits: runs the kernels' FP32->E4M3 encoder on
  *     the FP32 values whose bit patterns are first .. first+n-1, writing n
  *     codes to the device buffer `out`.
+ *   fp8bs_debug_split_plan: the split-K plan for `tiles` output tiles of
+ *     `kblocks` 128-wide contraction blocks on `sms` SMs, host only (no
+ *     device needed): out[0] splits (1 = none), out[1] the first split tile
+ *     (tiles before it are whole), out[2] work units, out[3] scratch bytes.
+ *     FP8BS_ERR_INVALID_ARG for non-positive sizes or a NULL `out`.
  */
 int fp8bs_debug_set_wait_timeout_ns(int64_t ns);
 int fp8bs_debug_set_fault(int mode);
 int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
+int fp8bs_debug_split_plan(int64_t tiles, int64_t kblocks, int sms, int64_t* out);
 
 #ifdef __cplusplus
 }

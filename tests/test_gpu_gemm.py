@@ -189,6 +189,45 @@ def test_wgrad_split_k_is_deterministic_and_within_tolerance():
     assert_gemm_close(np_bf16_bits(unsplit)[rows], acc, sab, "unsplit wgrad")
 
 
+@pytest.mark.parametrize("op", ["fprop", "dgrad"])
+def test_forward_and_data_gradient_tail_split(op):
+    """2432 x 2048 outputs (152 tiles of 128 x 256 = one full wave on 148 SMs
+    + 4 tiles), contraction 4096: the 4 tiles past the full wave (rows
+    2304-2431, columns 1024-2047) are split in 4 parts.  Repeated runs are
+    bitwise identical; the last 128 output rows and 64 random others meet the
+    acceptance rule, with and without the split."""
+    M, N, K = (2432, 2048, 4096) if op == "fprop" else (2432, 4096, 2048)
+    code = B.OP_FPROP if op == "fprop" else B.OP_DGRAD
+    assert B.fp8bs_gemm_workspace_bytes(code, M, N, K) > 0, "this shape should split"
+    x = inputs.random_bf16((M, K), seed=81)
+    w = inputs.random_bf16((N, K), seed=82, std=0.02)
+    dy = inputs.random_bf16((M, N), seed=83, std=1e-3)
+    wq, wqT, sw = B.fp8bs_quantize_weight(w.cuda(), want_t=True)
+    if op == "fprop":
+        aq, sa, _, _ = B.fp8bs_quantize_act(x.cuda(), B.ROWWISE)
+        run = lambda split: B.fp8bs_gemm_fprop(aq, sa, wq, sw, split=split)
+    else:
+        aq, sa, _, _ = B.fp8bs_quantize_act(dy.cuda(), B.ROWWISE)
+        run = lambda split: B.fp8bs_gemm_dgrad(aq, sa, wqT, sw, split=split)
+    runs = [run(True).view(torch.int16).clone() for _ in range(3)]
+    assert B.fp8bs_get_device_status() == 0
+    for r in runs[1:]:
+        assert torch.equal(r, runs[0])
+    B.fp8bs_set_workspace(None)
+    unsplit = run(False)
+    assert B.fp8bs_get_device_status() == 0
+    rows = np.concatenate([np.arange(M - 128, M), inputs.sample_rows(M - 128, 8181, 64).numpy()])
+    owq, _, osw = oracle.quant_weight_128x128(w, want_t=False)
+    if op == "fprop":
+        oaq, osa = oracle.quant_rowwise_1x128(x)
+        acc, _, sab = oracle_gemm_rows("fprop", oaq, osa, owq, osw, rows)
+    else:
+        oaq, osa = oracle.quant_rowwise_1x128(dy)
+        acc, _, sab = oracle_gemm_rows("dgrad", oaq, osa, owq, osw, rows)
+    assert_gemm_close(runs[0].cpu().numpy().view(np.uint16)[rows], acc, sab, f"split {op}")
+    assert_gemm_close(np_bf16_bits(unsplit)[rows], acc, sab, f"unsplit {op}")
+
+
 @pytest.mark.parametrize("M,N,K", [(384, 256, 640), (8192, 2048, 5632)])
 def test_wgrad_accumulates_in_fp32(M, N, K):
     """dW (FP32) += dY^T X, twice, starting from random FP32 values: every

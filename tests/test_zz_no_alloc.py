@@ -34,8 +34,9 @@ def _quantized_pair(M, N, K, seed):
 def test_noalloc_wgrad_matches_the_regular_entry_point_on_two_calls():
     assert torch.cuda.is_available()
     lib = B.load()
-    # 2048 x 5632 outputs = 352 tiles of 128 x 256: the tokens are split in two
-    # across CTAs, which needs ~44 MiB of scratch.
+    # 2048 x 5632 outputs = 352 tiles of 128 x 256 (2 full waves on 148 SMs
+    # + 56 tiles): the last 56 tiles' tokens are split in two across CTAs,
+    # which needs ~7 MiB of scratch.
     M, N, K = 8192, 2048, 5632
     need = B.fp8bs_gemm_wgrad_workspace_bytes(M, N, K)
     assert 0 < need <= SCRATCH_BYTES
@@ -59,8 +60,9 @@ def test_noalloc_wgrad_matches_the_regular_entry_point_on_two_calls():
 
 def test_noalloc_wgrad_rejects_shapes_that_need_more_scratch():
     lib = B.load()
-    # 1536 x 6400 outputs = 300 tiles: split four ways, ~113 MiB of scratch.
-    M, N, K = 16384, 1536, 6400
+    # 3968 x 2048 outputs = 248 tiles (1.7 waves on 148 SMs): every tile split
+    # four ways, ~93 MiB of scratch.
+    M, N, K = 16384, 3968, 2048
     assert B.fp8bs_gemm_wgrad_workspace_bytes(M, N, K) > SCRATCH_BYTES
     dyTq = torch.zeros(N, M, dtype=torch.uint8, device="cuda")
     xTq = torch.zeros(K, M, dtype=torch.uint8, device="cuda")
