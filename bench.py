@@ -538,6 +538,19 @@ def run_ours(args):
         result["cpu_baseline"] = {
             "value": fl / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": sample_note(args.cpu_feats, args.cpu_rows) + f", {sec:.1f} s"}
+    if not args.no_grouped:
+        from fp8_block_scaled_16_b300.linear import grouped_launch_list
+
+        gl = grouped_launch_list([(st, d["x"], d["w"], d.get("dy")) for st, d in steps_data])
+        time_step([gl], args.warmup, per_launch=False)
+        g_ms, _ = time_step([gl], args.steps, per_launch=False)
+        g_ms = D.max_over_ranks(ranks, g_ms / args.steps, device)
+        assert B.fp8bs_get_device_status() == 0, "device status after the grouped step"
+        result["grouped_step"] = {
+            "ms_per_step": round(g_ms, 4), "value": round(flops_step * ranks.world / (g_ms * 1e-3) / 1e12, 2),
+            "unit": UNIT, "launches_per_step": len(gl),
+            "note": "the same step with each GEMM phase of the four linears in one grouped launch "
+                    "(fp8bs_gemm_group: 4 forward, 4 data-gradient, 4 weight-gradient products; no split-K)"}
     if ranks.world == 1 and not args.no_bf16:
         bf_ms = bf16_comparison(wl, steps_data)
         result["bf16_comparison"] = {
@@ -594,7 +607,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=150)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
@@ -605,6 +618,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-grouped", action="store_true", help="skip the grouped-launch step")
     ap.add_argument("--no-bf16", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -17,7 +17,7 @@ _BINDING_NAMES = (
     "fp8bs_debug_set_wait_timeout_ns", "fp8bs_debug_set_fault", "fp8bs_debug_e4m3_encode_bits",
     "fp8bs_debug_split_plan",
     "fp8bs_set_workspace", "fp8bs_gemm_workspace_bytes", "fp8bs_gemm_wgrad_workspace_bytes",
-    "fp8bs_gemm_wgrad_noalloc", "OP_FPROP", "OP_DGRAD", "OP_WGRAD",
+    "fp8bs_gemm_wgrad_noalloc", "OP_FPROP", "OP_DGRAD", "OP_WGRAD", "fp8bs_gemm_group", "GemmArgs",
     "fp8bs_gemm_wgrad_accumulate_f32",
 )
 

@@ -31,6 +31,15 @@ STATUS = {
 # Every symbol include/fp8bs.h declares, with its ctypes signature.
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
+class GemmArgs(ctypes.Structure):
+    """fp8bs_gemm_args: one member of a grouped GEMM."""
+    _fields_ = [("op", ctypes.c_int), ("a", ctypes.c_void_p), ("sa", ctypes.c_void_p), ("b", ctypes.c_void_p),
+                ("sb", ctypes.c_void_p), ("out", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64)]
+
+
+GROUP_MAX = 4  # FP8BS_GROUP_MAX
+
 SIGNATURES = {
     "fp8bs_quantize_act": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_uint, _P, _P, _P, _P, _P]),
     "fp8bs_quantize_weight": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
@@ -40,6 +49,7 @@ SIGNATURES = {
     "fp8bs_get_device_status": (ctypes.c_int, [_P]),
     "fp8bs_set_workspace": (ctypes.c_int, [_P, _I64]),
     "fp8bs_gemm_workspace_bytes": (_I64, [ctypes.c_int, _I64, _I64, _I64]),
+    "fp8bs_gemm_group": (ctypes.c_int, [ctypes.POINTER(GemmArgs), ctypes.c_int, _P]),
     "fp8bs_debug_split_plan": (ctypes.c_int, [_I64, _I64, ctypes.c_int, _P]),
     "fp8bs_gemm_wgrad_workspace_bytes": (_I64, [_I64, _I64, _I64]),
     "fp8bs_gemm_wgrad_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -310,3 +320,36 @@ def fp8bs_debug_split_plan(tiles: int, kblocks: int, sms: int) -> dict:
     _check(load().fp8bs_debug_split_plan(tiles, kblocks, sms, ctypes.cast(out, ctypes.c_void_p)),
            "fp8bs_debug_split_plan")
     return {"splits": out[0], "tail_first": out[1], "units": out[2], "bytes": out[3]}
+
+
+def fp8bs_gemm_group(members, stream=None):
+    """Several products in one launch.  `members` lists (op, a, sa, b, sb,
+    out) with op OP_FPROP (a = Xq, sa = sx, b = Wq, sb = sw), OP_DGRAD (dYq,
+    sdy, WqT, sw) or OP_WGRAD (dYTq, sdyT, XTq, sxT), operand layouts as for
+    that op's own function; `out` may be None (allocated).  Forward and
+    data-gradient products may share a group, weight gradients group alone.
+    Returns the outputs in order; each equals the op's unsplit result."""
+    if not 1 <= len(members) <= GROUP_MAX:
+        raise ValueError(f"a group has 1..{GROUP_MAX} members, got {len(members)}")
+    arr = (GemmArgs * len(members))()
+    outs = []
+    for i, (op, a, sa, b, sb, out) in enumerate(members):
+        if op == OP_FPROP:
+            (M, K), N = a.shape, b.shape[0]
+            shapes = ((M, K), (K // 128, padded_tokens(M)), (N, K), (N // 128, K // 128), (M, N))
+        elif op == OP_DGRAD:
+            (M, N), K = a.shape, b.shape[0]
+            shapes = ((M, N), (N // 128, padded_tokens(M)), (K, N), (N // 128, K // 128), (M, K))
+        elif op == OP_WGRAD:
+            (N, Mp), K = a.shape, b.shape[0]
+            M = Mp
+            shapes = ((N, Mp), (Mp // 128, N), (K, Mp), (Mp // 128, K), (N, K))
+        else:
+            raise ValueError(f"unknown op {op}")
+        out = _out(out, shapes[4], torch.bfloat16, a.device)
+        arr[i] = GemmArgs(op, _dev(a, torch.uint8, shapes[0], "a"), _dev(sa, torch.float32, shapes[1], "sa"),
+                          _dev(b, torch.uint8, shapes[2], "b"), _dev(sb, torch.float32, shapes[3], "sb"),
+                          _dev(out, torch.bfloat16, shapes[4], "out"), M, N, K)
+        outs.append(out)
+    _check(load().fp8bs_gemm_group(arr, len(members), _stream(stream)), "fp8bs_gemm_group")
+    return outs

@@ -40,7 +40,7 @@ struct DeviceInfo {
     bool arch_ok = false;
     int sm_count = 0;
     uint32_t* status = nullptr;
-    bool gemm_attr_set[2] = {false, false};
+    bool gemm_attr_set[2][2] = {{false, false}, {false, false}};  // [scale mode][grouped]
     // Caller-registered scratch for split-K GEMMs (fp8bs_set_workspace).
     uint8_t* ws = nullptr;
     int64_t ws_bytes = 0;
@@ -181,46 +181,112 @@ SplitPlan plan_splits(int64_t tiles, int64_t kblocks, int sms) {
     return best;
 }
 
-template <int SBMODE, int BN>
-int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
-                const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
-                cudaStream_t st, bool out_f32_add = false) {
+// One product in the kernel's operand roles: C[rows][cols] = A[rows][kc] *
+// B[cols][kc]^T with row scales sa [kc/128][padded rows] and B scales
+// either scalar (sb[jb * sb_stride_j + b * sb_stride_b]) or per column
+// (sb [kc/128][cols]).
+struct GemmSpec {
+    int sbmode;
+    const uint8_t* A;
+    const uint8_t* B;
+    int64_t rows, cols, kc;
+    const float* sa;
+    const float* sb;
+    int64_t sb_stride_j, sb_stride_b;
+    void* out;
+    bool out_f32_add;
+};
+
+// The operand roles of product `op` called with its entry point's arguments.
+GemmSpec spec_of(int op, const uint8_t* a, const float* sa, const uint8_t* b, const float* sb, void* out,
+                 int64_t M, int64_t N, int64_t K, bool out_f32_add = false) {
+    switch (op) {
+        case FP8BS_OP_FPROP:
+            // A = Xq [M][K] (row scales sx [K/128][Mp]); B = Wq [N][K]; the B scale of
+            // output column block jb and K block b is sw[jb][b].
+            return {gemm::SB_SCALAR, a, b, M, N, K, sa, sb, K / 128, 1, out, false};
+        case FP8BS_OP_DGRAD:
+            // A = dYq [M][N] (row scales sdy [N/128][Mp]); B = WqT [K][N]; contraction
+            // block b is a 128-row block of W, output column block jb a 128-column
+            // block of W: scale sw[b][jb].
+            return {gemm::SB_SCALAR, a, b, M, K, N, sa, sb, 1, K / 128, out, false};
+        default:
+            // A = dYTq [N][Mp] (row scales sdyT [Mp/128][N]); B = XTq [K][Mp] with a
+            // per-column scale vector sxT [Mp/128][K].  Contraction over the tokens,
+            // padded to whole 128-token blocks (the transposed quantizer writes zero
+            // payloads for the padding).
+            return {gemm::SB_VECTOR, a, b, N, K, padded_tokens(M), sa, sb, 0, 0, out, out_f32_add};
+    }
+}
+
+// Tensor maps and kernel parameters of one product, not split.
+int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmC,
+                gemm::Params* p) {
     using namespace gemm;
-    using T = Tile<BN>;
-    CUtensorMap tmA, tmB, tmC;
-    if (!tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kc, rows, kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kc, cols, kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !(out_f32_add ? tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, cols, rows, cols * 4, 32, 32,
-                                CU_TENSOR_MAP_SWIZZLE_128B)
-                      : tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, cols, rows, cols * 2, 64, 32,
-                                CU_TENSOR_MAP_SWIZZLE_128B)))
+    constexpr int BN = 256;
+    if (!tmap_2d(tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.A, s.kc, s.rows, s.kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tmap_2d(tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.B, s.kc, s.cols, s.kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !(s.out_f32_add ? tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, s.out, s.cols, s.rows, s.cols * 4, 32, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_128B)
+                        : tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.out, s.cols, s.rows, s.cols * 2, 64, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_128B)))
         return FP8BS_ERR_LAUNCH;
+    p->out_f32_add = s.out_f32_add ? 1 : 0;
+    p->m_tiles = static_cast<int32_t>((s.rows + BM - 1) / BM);
+    p->sa_ld = padded_tokens(s.rows);
+    p->n_tiles = static_cast<int32_t>((s.cols + BN - 1) / BN);
+    p->kblocks = static_cast<int32_t>(s.kc / BK);
+    p->nb_valid = static_cast<int32_t>(s.cols / 128);
+    p->rows = s.rows;
+    p->cols = s.cols;
+    p->sa = s.sa;
+    p->sb = s.sb;
+    p->sb_stride_j = s.sb_stride_j;
+    p->sb_stride_b = s.sb_stride_b;
+    p->out = static_cast<uint16_t*>(s.out);
+    p->status = d->status;
+    p->timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
+    p->fault = 0;
+    p->splits = 1;
+    p->tail_first = 0;
+    p->ws = nullptr;
+    p->flags = nullptr;
+    p->epoch = 0;
+    if (static_cast<int64_t>(p->m_tiles) * p->n_tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
+    return FP8BS_OK;
+}
 
-    Params p;
-    p.out_f32_add = out_f32_add ? 1 : 0;
-    p.m_tiles = static_cast<int32_t>((rows + BM - 1) / BM);
-    p.sa_ld = padded_tokens(rows);
-    p.n_tiles = static_cast<int32_t>((cols + BN - 1) / BN);
-    p.kblocks = static_cast<int32_t>(kc / BK);
-    p.nb_valid = static_cast<int32_t>(cols / 128);
-    p.rows = rows;
-    p.cols = cols;
-    p.sa = sa;
-    p.sb = sb;
-    p.sb_stride_j = sb_stride_j;
-    p.sb_stride_b = sb_stride_b;
-    p.out = static_cast<uint16_t*>(out);
-    p.status = d->status;
-    p.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
+template <int SBMODE, int G>
+int launch_group(DeviceInfo* d, const gemm::Group<G>& grp, cudaStream_t st) {
+    using namespace gemm;
+    using T = Tile<256>;
+    const int64_t units = grp.first_unit[grp.count];
+    if (units <= 0) return FP8BS_OK;
+    const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
+    auto kern = gemm_kernel<SBMODE, 256, G>;
+    bool& attr = d->gemm_attr_set[SBMODE][G > 1 ? 1 : 0];
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
+            return launch_status();
+        attr = true;
+    }
+    kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(grp);
+    g_launches.fetch_add(1);
+    return launch_status();
+}
+
+// One product, split along K when the registered scratch allows a plan that pays.
+int run_gemm(const GemmSpec& s, cudaStream_t st) {
+    using namespace gemm;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    Group<1> grp;
+    Params& p = grp.p[0];
+    rc = fill_member(d, s, &grp.tmA[0], &grp.tmB[0], &grp.tmC[0], &p);
+    if (rc != FP8BS_OK) return rc;
     p.fault = g_fault.exchange(0);
-    p.splits = 1;
-    p.tail_first = 0;
-    p.ws = nullptr;
-    p.flags = nullptr;
-    p.epoch = 0;
-
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    if (tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
     int64_t units = tiles;
     if (d->ws != nullptr) {
         const SplitPlan sp = plan_splits(tiles, p.kblocks, d->sm_count);
@@ -233,30 +299,10 @@ int launch_gemm(DeviceInfo* d, const uint8_t* A, const uint8_t* B, int64_t rows,
             units = sp.units;
         }
     }
-    const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
-
-    auto kern = gemm_kernel<SBMODE, BN>;
-    if (!d->gemm_attr_set[SBMODE]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
-            return launch_status();
-        d->gemm_attr_set[SBMODE] = true;
-    }
-    kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(tmA, tmB, tmC, p);
-    g_launches.fetch_add(1);
-    return launch_status();
-}
-
-// C[rows][cols] = block-scaled A[rows][kc] * B[cols][kc]^T (see gemm.cuh).
-int run_gemm(int sbmode, const uint8_t* A, const uint8_t* B, int64_t rows, int64_t cols, int64_t kc,
-             const float* sa, const float* sb, int64_t sb_stride_j, int64_t sb_stride_b, void* out,
-             cudaStream_t st, bool out_f32_add = false) {
-    DeviceInfo* d = nullptr;
-    int rc = current_device(&d);
-    if (rc != FP8BS_OK) return rc;
-    if (sbmode == gemm::SB_VECTOR)
-        return launch_gemm<gemm::SB_VECTOR, 256>(d, A, B, rows, cols, kc, sa, sb, sb_stride_j, sb_stride_b, out, st,
-                                                 out_f32_add);
-    return launch_gemm<gemm::SB_SCALAR, 256>(d, A, B, rows, cols, kc, sa, sb, sb_stride_j, sb_stride_b, out, st);
+    grp.count = 1;
+    grp.first_unit[0] = 0;
+    grp.first_unit[1] = static_cast<int32_t>(units);
+    return s.sbmode == SB_VECTOR ? launch_group<SB_VECTOR, 1>(d, grp, st) : launch_group<SB_SCALAR, 1>(d, grp, st);
 }
 
 }  // namespace
@@ -317,39 +363,66 @@ int fp8bs_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, cons
                      int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(xq, sx, wq, sw, y, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    // A = Xq [M][K] (row scales sx [K/128][M]); B = Wq [N][K]; the B scale of
-    // output column block jb and K block b is sw[jb][b].
-    return run_gemm(gemm::SB_SCALAR, xq, wq, M, N, K, sx, sw, K / 128, 1, y, static_cast<cudaStream_t>(stream));
+    return run_gemm(spec_of(FP8BS_OP_FPROP, xq, sx, wq, sw, y, M, N, K), static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw, void* dx,
                      int64_t M, int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(dyq, sdy, wqT, sw, dx, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    // A = dYq [M][N] (row scales sdy [N/128][M]); B = WqT [K][N]; contraction
-    // block b is a 128-row block of W, output column block jb a 128-column
-    // block of W: scale sw[b][jb].
-    return run_gemm(gemm::SB_SCALAR, dyq, wqT, M, K, N, sdy, sw, 1, K / 128, dx, static_cast<cudaStream_t>(stream));
+    return run_gemm(spec_of(FP8BS_OP_DGRAD, dyq, sdy, wqT, sw, dx, M, N, K), static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT, void* dw,
                      int64_t M, int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    // A = dYTq [N][M] (row scales sdyT [M/128][N]); B = XTq [K][M] with a
-    // per-column scale vector sxT [M/128][K].
-    // Contraction over the tokens, padded to whole 128-token blocks (the
-    // transposed quantizer writes zero payloads for the padding).
-    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, padded_tokens(M), sdyT, sxT, 0, 0, dw,
-                    static_cast<cudaStream_t>(stream));
+    return run_gemm(spec_of(FP8BS_OP_WGRAD, dyTq, sdyT, xTq, sxT, dw, M, N, K), static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
                                     float* dw, int64_t M, int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    return run_gemm(gemm::SB_VECTOR, dyTq, xTq, N, K, padded_tokens(M), sdyT, sxT, 0, 0, dw,
-                    static_cast<cudaStream_t>(stream), true);
+    return run_gemm(spec_of(FP8BS_OP_WGRAD, dyTq, sdyT, xTq, sxT, dw, M, N, K, true),
+                    static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_gemm_group(const fp8bs_gemm_args* gemms, int count, void* stream) {
+    using namespace gemm;
+    static_assert(kGroupMax == FP8BS_GROUP_MAX, "group size");
+    static_assert(sizeof(Group<kGroupMax>) <= 4096, "kernel parameter space");
+    if (gemms == nullptr || count < 1 || count > FP8BS_GROUP_MAX) return FP8BS_ERR_INVALID_ARG;
+    int sbmode = -1;
+    for (int i = 0; i < count; i++) {
+        const fp8bs_gemm_args& a = gemms[i];
+        if (a.op != FP8BS_OP_FPROP && a.op != FP8BS_OP_DGRAD && a.op != FP8BS_OP_WGRAD) return FP8BS_ERR_INVALID_ARG;
+        const int rc = check_gemm_args(a.a, a.sa, a.b, a.sb, a.out, a.M, a.N, a.K);
+        if (rc != FP8BS_OK) return rc;
+        const int mode = a.op == FP8BS_OP_WGRAD ? SB_VECTOR : SB_SCALAR;
+        if (sbmode >= 0 && mode != sbmode) return FP8BS_ERR_INVALID_ARG;
+        sbmode = mode;
+    }
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    Group<kGroupMax> grp;
+    grp.count = count;
+    grp.first_unit[0] = 0;
+    for (int i = 0; i < count; i++) {
+        const fp8bs_gemm_args& a = gemms[i];
+        rc = fill_member(d, spec_of(a.op, a.a, a.sa, a.b, a.sb, a.out, a.M, a.N, a.K), &grp.tmA[i], &grp.tmB[i],
+                         &grp.tmC[i], &grp.p[i]);
+        if (rc != FP8BS_OK) return rc;
+        const int64_t end = grp.first_unit[i] + static_cast<int64_t>(grp.p[i].m_tiles) * grp.p[i].n_tiles;
+        if (end > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
+        grp.first_unit[i + 1] = static_cast<int32_t>(end);
+    }
+    for (int i = count; i < kGroupMax; i++) grp.first_unit[i + 1] = grp.first_unit[count];
+    grp.p[0].fault = g_fault.exchange(0);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return sbmode == SB_VECTOR ? launch_group<SB_VECTOR, kGroupMax>(d, grp, st)
+                               : launch_group<SB_SCALAR, kGroupMax>(d, grp, st);
 }
 
 int fp8bs_set_workspace(void* ws, int64_t bytes) {
@@ -371,6 +444,7 @@ int fp8bs_set_workspace(void* ws, int64_t bytes) {
 }
 
 int64_t fp8bs_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+    if (op != FP8BS_OP_FPROP && op != FP8BS_OP_DGRAD && op != FP8BS_OP_WGRAD) return -FP8BS_ERR_INVALID_ARG;
     if (!tokens_ok(M) || !dim_ok(N) || !dim_ok(K)) return -FP8BS_ERR_SHAPE;
     DeviceInfo* d = nullptr;
     int rc = current_device(&d);
@@ -394,7 +468,6 @@ int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
                              void* dw, int64_t M, int64_t N, int64_t K, void* stream) {
     using namespace gemm;
-    using T = Tile<256>;
     int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
     if (rc != FP8BS_OK) return rc;
     DeviceInfo* d = nullptr;
@@ -421,36 +494,12 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
     const SplitPlan sp = plan_splits(tiles, kc / BK, d->sm_count);
     if (sp.bytes > static_cast<int64_t>(FP8BS_NOALLOC_SCRATCH_BYTES)) return FP8BS_ERR_SHAPE;
 
-    CUtensorMap tmA, tmB, tmC;
-    if (!tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, dyTq, kc, rows, kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, xTq, kc, cols, kc, BK, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dw, cols, rows, cols * 2, 64, 32,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-        return FP8BS_ERR_LAUNCH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-    Params p;
-    p.m_tiles = static_cast<int32_t>(rows / BM);
-    p.sa_ld = rows;
-    p.n_tiles = static_cast<int32_t>((cols + 255) / 256);
-    p.kblocks = static_cast<int32_t>(kc / BK);
-    p.nb_valid = static_cast<int32_t>(cols / 128);
-    p.rows = rows;
-    p.cols = cols;
-    p.sa = sdyT;
-    p.sb = sxT;
-    p.sb_stride_j = 0;
-    p.sb_stride_b = 0;
-    p.out = static_cast<uint16_t*>(dw);
-    p.status = d->status;
-    p.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
-    p.fault = 0;
-    p.out_f32_add = 0;
-    p.splits = sp.splits;
-    p.tail_first = static_cast<int32_t>(sp.tail_first);
-    p.ws = nullptr;
-    p.flags = nullptr;
-    p.epoch = 0;
+    Group<1> grp;
+    Params& p = grp.p[0];
+    rc = fill_member(d, spec_of(FP8BS_OP_WGRAD, dyTq, sdyT, xTq, sxT, dw, M, N, K), &grp.tmA[0], &grp.tmB[0],
+                     &grp.tmC[0], &p);
+    if (rc != FP8BS_OK) return rc;
     if (sp.splits > 1) {
         // The scratch keeps whatever the previous call left: clear the flags
         // this call will use (partials are always written before they are read).
@@ -459,18 +508,16 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
             cudaGetLastError();
             return FP8BS_ERR_LAUNCH;
         }
+        p.splits = sp.splits;
+        p.tail_first = static_cast<int32_t>(sp.tail_first);
         p.flags = reinterpret_cast<uint32_t*>(d->noalloc_scratch);
         p.ws = reinterpret_cast<float*>(d->noalloc_scratch + kFlagBytes);
         p.epoch = 1;
     }
-    const int64_t units = sp.units;
-    const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
-    auto kern = gemm_kernel<SB_VECTOR, 256>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
-        return launch_status();
-    kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(tmA, tmB, tmC, p);
-    g_launches.fetch_add(1);
-    return launch_status();
+    grp.count = 1;
+    grp.first_unit[0] = 0;
+    grp.first_unit[1] = static_cast<int32_t>(sp.units);
+    return launch_group<SB_VECTOR, 1>(d, grp, st);
 }
 
 int fp8bs_get_device_status(void* stream) {

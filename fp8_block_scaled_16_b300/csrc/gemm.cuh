@@ -181,6 +181,29 @@ __device__ __forceinline__ Unit unit_of(int u, const Params& p, int num_tiles) {
     return w;
 }
 
+// Up to G products computed by one persistent launch: member g owns the
+// work units [first_unit[g], first_unit[g+1]) (its own units numbered as in
+// unit_of).  A single product is a group of one.  Every member of a group
+// has the same scale mode (the kernel's SBMODE).
+constexpr int kGroupMax = 4;
+template <int G>
+struct Group {
+    CUtensorMap tmA[G], tmB[G], tmC[G];
+    Params p[G];
+    int32_t count;
+    int32_t first_unit[G + 1];
+};
+template <int G>
+__device__ __forceinline__ int member_of(const Group<G>& grp, int u) {
+    int g = 0;
+    if constexpr (G > 1) {
+#pragma unroll
+        for (int i = 1; i < G; i++)
+            if (i < grp.count && u >= grp.first_unit[i]) g = i;
+    }
+    return g;
+}
+
 // Waits (bounded) until a helper's flag carries this launch's epoch.
 __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, const WaitCtx& w) {
     const uint64_t t0 = global_timer_ns();
@@ -284,10 +307,8 @@ __device__ __forceinline__ void promote_rank1(float (&acc)[N], int base_lo, int 
     }
 }
 
-template <int SBMODE, int BN>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const Params p) {
+template <int SBMODE, int BN, int G>
+__global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ Group<G> grp) {
     using T = Tile<BN>;
     constexpr int STAGES = T::STAGES, NBUF = T::NBUF, COLS = T::COLS;
     extern __shared__ uint8_t smem_raw[];
@@ -316,9 +337,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmC);
+        for (int g = 0; g < grp.count; g++) {
+            tma_prefetch_desc(&grp.tmA[g]);
+            tma_prefetch_desc(&grp.tmB[g]);
+            tma_prefetch_desc(&grp.tmC[g]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&misc[0]), TMEM_COLS);
@@ -329,9 +352,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
 
     const uint32_t tmem = misc[0];
-    const WaitCtx wc{reinterpret_cast<volatile uint32_t*>(&misc[1]), p.status, p.timeout_ns};
-    const int num_tiles = p.m_tiles * p.n_tiles;
-    const int num_units = num_units_of(p, num_tiles);
+    const Params& p0 = grp.p[0];   // status word, time limit and test hook are the group's
+    const WaitCtx wc{reinterpret_cast<volatile uint32_t*>(&misc[1]), p0.status, p0.timeout_ns};
+    const int num_units = grp.first_unit[grp.count];
+    // Work unit u: its member's parameters, tile count and (tile, K range).
+#define FP8BS_UNIT(u)                                          \
+    const int g = member_of(grp, u);                           \
+    const Params& p = grp.p[g];                                \
+    const int num_tiles = p.m_tiles * p.n_tiles;               \
+    const Unit w = unit_of((u) - grp.first_unit[g], p, num_tiles)
 
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
@@ -347,17 +376,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t armed = 0, armed_par = 0, inj = 0;      // per stage
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-            const Unit w = unit_of(u, p, num_tiles);
+            FP8BS_UNIT(u);
             const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
             for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::empty(stage)), ph ^ 1u, wc)) { ok = false; break; }
-                const bool inject = p.fault != 0 && blockIdx.x == 0 && u == static_cast<int>(blockIdx.x) && kb == w.kb0;
+                const bool inject = p0.fault != 0 && blockIdx.x == 0 && u == static_cast<int>(blockIdx.x) && kb == w.kb0;
                 if (lane == 0) {
                     const uint32_t fb = bar(T::full(stage));
                     mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
                     if (!inject) {
-                        tma_load_2d(sbase + T::OFF_A + stage * T::A_BYTES, &tmA, kb * BK, mb * BM, fb);
-                        tma_load_2d(sbase + T::OFF_B + stage * T::B_BYTES, &tmB, kb * BK, nb * BN, fb);
+                        tma_load_2d(sbase + T::OFF_A + stage * T::A_BYTES, &grp.tmA[g], kb * BK, mb * BM, fb);
+                        tma_load_2d(sbase + T::OFF_B + stage * T::B_BYTES, &grp.tmB[g], kb * BK, nb * BN, fb);
                     }
                 }
                 __syncwarp();
@@ -371,7 +400,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // Let every copy this CTA issued land before it exits.
             for (int s = 0; s < STAGES; s++)
                 if (((armed >> s) & 1u) && !((inj >> s) & 1u))
-                    drain_wait(bar(T::full(s)), (armed_par >> s) & 1u, p.timeout_ns);
+                    drain_wait(bar(T::full(s)), (armed_par >> s) & 1u, p0.timeout_ns);
         }
         __syncwarp();
       } else if (warp == 1) {
@@ -383,7 +412,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int last_tb = 0;
         uint32_t last_tph = 0;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-            const Unit w = unit_of(u, p, num_tiles);
+            FP8BS_UNIT(u);
+            (void)num_tiles;
             for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
                 if (!warp_wait_bounded(bar(T::full(stage)), ph, wc)) { ok = false; break; }
@@ -407,7 +437,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (++tb == NBUF) { tb = 0; tph ^= 1u; }
             }
         }
-        if (!ok && issued && lane == 0) drain_wait(bar(T::tfull(last_tb)), last_tph, p.timeout_ns);
+        if (!ok && issued && lane == 0) drain_wait(bar(T::tfull(last_tb)), last_tph, p0.timeout_ns);
         __syncwarp();
       } else if (warp == 2) {
         // ------------------------------------------------ scale loader
@@ -416,7 +446,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true;
         const uint32_t ring = sbase + T::OFF_SCALE;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-            const Unit w = unit_of(u, p, num_tiles);
+            FP8BS_UNIT(u);
             const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
             for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::sempty(slot)), sph ^ 1u, wc)) { ok = false; break; }
@@ -465,7 +495,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t tph = 0, sph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-            const Unit w = unit_of(u, p, num_tiles);
+            FP8BS_UNIT(u);
             const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
             // 128-column block of the output this warp's columns fall in
             const int jb = (nb * BN + half * COLS) >> 7;
@@ -629,8 +659,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     __syncwarp();
                     if (lane == 0) {
                         const int32_t x0 = nb * BN + half * COLS + h * 64, y0 = mb * BM + quad * 32;
-                        tma_reduce_add_2d(&tmC, stage_out, x0, y0);
-                        tma_reduce_add_2d(&tmC, stage_out + T::OUT_BOX_BYTES, x0 + 32, y0);
+                        tma_reduce_add_2d(&grp.tmC[g], stage_out, x0, y0);
+                        tma_reduce_add_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, x0 + 32, y0);
                         bulk_commit_group();
                     }
                 }
@@ -684,8 +714,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     const int32_t x0 = nb * BN + half * COLS, y0 = mb * BM + quad * 32;
-                    tma_store_2d(&tmC, stage_out, x0, y0);
-                    tma_store_2d(&tmC, stage_out + T::OUT_BOX_BYTES, x0 + 64, y0);
+                    tma_store_2d(&grp.tmC[g], stage_out, x0, y0);
+                    tma_store_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, x0 + 64, y0);
                     bulk_commit_group();
                 }
             }
@@ -694,6 +724,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     }
 
+#undef FP8BS_UNIT
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

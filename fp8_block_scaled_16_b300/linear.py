@@ -92,3 +92,37 @@ class Fp8LinearStep:
         for launch in self.launch_list(x, w, dy, stream=stream):
             launch.run()
         return self.y, self.dx, self.dw
+
+
+def grouped_launch_list(steps, stream=None) -> List[Launch]:
+    """One training step of several independent linears (e.g. a decoder
+    layer's four) with each GEMM phase in one grouped launch.  `steps` lists
+    (Fp8LinearStep, x, w, dy): the quantizations run per linear as in
+    launch_list; then one launch computes every forward product, one every
+    data gradient and one every weight gradient (fp8bs_gemm_group).  The
+    outputs are bitwise those of the linears' own launch lists without
+    split-K."""
+    if len(steps) > B.GROUP_MAX:
+        raise ValueError(f"at most {B.GROUP_MAX} linears per group")
+    quant_x, quant_dy, fprop, dgrad, wgrad = [], [], [], [], []
+    for st, x, w, dy in steps:
+        single = st.launch_list(x, w, dy, stream=stream)
+        quant_x += [l for l in single if l.op == "quant_weight" or (l.op == "quant_act" and l is single[0])]
+        quant_dy += [l for l in single if l.op == "quant_act" and l is not single[0]]
+        fl = 2 * st.M * st.N * st.K
+        fprop.append(((B.OP_FPROP, st.xq, st.sx, st.wq, st.sw, st.y), fl))
+        if "dgrad" in st.ops:
+            dgrad.append(((B.OP_DGRAD, st.dyq, st.sdy, st.wqT, st.sw, st.dx), fl))
+        if "wgrad" in st.ops:
+            wgrad.append(((B.OP_WGRAD, st.dyTq, st.sdyT, st.xTq, st.sxT, st.dw), fl))
+
+    def group(op, members):
+        args = [m for m, _ in members]
+        return Launch(op, sum(f for _, f in members), "flops", lambda: B.fp8bs_gemm_group(args, stream=stream))
+
+    out = quant_x + [group("fprop", fprop)] + quant_dy
+    if dgrad:
+        out.append(group("dgrad", dgrad))
+    if wgrad:
+        out.append(group("wgrad", wgrad))
+    return out

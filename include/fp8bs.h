@@ -161,6 +161,46 @@ int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq,
 int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
                                     float* dw, int64_t M, int64_t N, int64_t K, void* stream);
 
+/* Product codes of fp8bs_gemm_group and fp8bs_gemm_workspace_bytes. */
+#define FP8BS_OP_FPROP 0
+#define FP8BS_OP_DGRAD 1
+#define FP8BS_OP_WGRAD 2
+
+/*
+ * Several products in one persistent launch (grouped GEMM).
+ *
+ * A decoder layer's linears give independent products of the same kind in
+ * each phase of a step -- the forward products of its four linears, their
+ * data gradients, their weight gradients.  Launched one by one, each ends
+ * with a partly idle last wave of its 128 x 256 tiles; grouped, the tiles of
+ * all members are dealt to the persistent CTAs as one list (member 0's tiles
+ * first), so only the group's last wave is ragged.
+ *   gemms[count] : 1 <= count <= FP8BS_GROUP_MAX products, each given by its
+ *                  op (FP8BS_OP_FPROP, _DGRAD or _WGRAD) and exactly the
+ *                  arguments of that op's entry point (a = xq / dyq / dyTq,
+ *                  sa = sx / sdy / sdyT, b = wq / wqT / xTq, sb = sw / sw /
+ *                  sxT, out = y / dx / dw as BF16).  Forward and data-gradient
+ *                  products may share a group; weight gradients form groups
+ *                  of their own (their promotion differs).
+ * Each output is bitwise equal to the unsplit result of the member's own
+ * entry point (no split-K inside a group).  Outputs must not overlap each
+ * other or any input.  Errors: FP8BS_ERR_INVALID_ARG for a NULL array, a
+ * count out of range, an unknown op or mixed weight-gradient and other
+ * members; otherwise as for the members' entry points (checked before
+ * anything is launched).
+ */
+#define FP8BS_GROUP_MAX 4
+typedef struct fp8bs_gemm_args {
+    int op;
+    const uint8_t* a;
+    const float* sa;
+    const uint8_t* b;
+    const float* sb;
+    void* out;
+    int64_t M, N, K;
+} fp8bs_gemm_args;
+int fp8bs_gemm_group(const fp8bs_gemm_args* gemms, int count, void* stream);
+
 /*
  * Scratch memory for the GEMMs' split-K path (caller-owned).
  *
@@ -187,9 +227,6 @@ int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, cons
  *     registration a product simply does not split.  GEMMs that share one
  *     scratch must not overlap in time (two streams would race on it).
  */
-#define FP8BS_OP_FPROP 0
-#define FP8BS_OP_DGRAD 1
-#define FP8BS_OP_WGRAD 2
 int fp8bs_set_workspace(void* ws, int64_t bytes);
 int64_t fp8bs_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
 int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K);

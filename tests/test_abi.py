@@ -88,6 +88,31 @@ def test_validation_before_launch(lib):
     assert lib.fp8bs_gemm_wgrad_workspace_bytes(128, 0, 128) == -2
 
 
+def test_group_validation_before_launch(lib):
+    fake = 0x10000
+    good = B.GemmArgs(B.OP_FPROP, fake, fake, fake, fake, fake, 128, 256, 128)
+    wgrad = B.GemmArgs(B.OP_WGRAD, fake, fake, fake, fake, fake, 128, 256, 128)
+    bad_op = B.GemmArgs(7, fake, fake, fake, fake, fake, 128, 256, 128)
+    bad_shape = B.GemmArgs(B.OP_DGRAD, fake, fake, fake, fake, fake, 128, 200, 128)
+    null_out = B.GemmArgs(B.OP_FPROP, fake, fake, fake, fake, None, 128, 256, 128)
+    odd = B.GemmArgs(B.OP_FPROP, fake, fake, fake + 8, fake, fake, 128, 256, 128)
+
+    def call(*members, count=None):
+        arr = (B.GemmArgs * max(1, len(members)))(*members)
+        return lib.fp8bs_gemm_group(arr, len(members) if count is None else count, None)
+
+    assert lib.fp8bs_gemm_group(None, 1, None) == 1
+    assert call(good, count=0) == 1
+    assert call(good, good, good, good, good) == 1              # more than FP8BS_GROUP_MAX
+    assert call(good, bad_op) == 1
+    assert call(good, wgrad) == 1                               # weight gradients group alone
+    assert call(good, null_out) == 1
+    assert call(bad_shape) == 2
+    assert call(good, odd) == 3
+    assert lib.fp8bs_gemm_workspace_bytes(9, 128, 256, 128) == -1   # unknown product
+    assert lib.fp8bs_gemm_workspace_bytes(B.OP_FPROP, 0, 256, 128) == -2
+
+
 def test_debug_setters(lib):
     assert lib.fp8bs_debug_set_fault(2) == 1
     assert lib.fp8bs_debug_set_fault(0) == 0

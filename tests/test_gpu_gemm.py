@@ -228,6 +228,47 @@ def test_forward_and_data_gradient_tail_split(op):
     assert_gemm_close(np_bf16_bits(unsplit)[rows], acc, sab, f"unsplit {op}")
 
 
+def test_grouped_launch_equals_single_launches():
+    """Products of different shapes (a token tail, ragged output tiles) in
+    one launch: forward and data-gradient products together, weight
+    gradients in a group of their own.  Every output is bitwise equal to the
+    member's own unsplit call; one member of each group is also checked
+    against the oracle on all of its outputs."""
+    B.fp8bs_set_workspace(None)  # single calls unsplit, like group members
+    shapes = [(300, 384, 640), (1024, 1536, 768), (512, 256, 1280)]  # (tokens M, out N, in K)
+    ops = []
+    for i, (M, N, K) in enumerate(shapes):
+        x = inputs.random_bf16((M, K), seed=90 + i)
+        w = inputs.random_bf16((N, K), seed=95 + i, std=0.02)
+        dy = inputs.random_bf16((M, N), seed=99 + i, std=1e-3)
+        xq, sx, xTq, sxT = B.fp8bs_quantize_act(x.cuda(), B.ROWWISE | B.COLWISE_T)
+        wq, wqT, sw = B.fp8bs_quantize_weight(w.cuda(), want_t=True)
+        dyq, sdy, dyTq, sdyT = B.fp8bs_quantize_act(dy.cuda(), B.ROWWISE | B.COLWISE_T)
+        ops.append(dict(x=x, w=w, dy=dy, xq=xq, sx=sx, xTq=xTq, sxT=sxT, wq=wq, wqT=wqT, sw=sw, dyq=dyq,
+                        sdy=sdy, dyTq=dyTq, sdyT=sdyT))
+    fwd = [(B.OP_FPROP, o["xq"], o["sx"], o["wq"], o["sw"], None) for o in ops] + \
+          [(B.OP_DGRAD, ops[1]["dyq"], ops[1]["sdy"], ops[1]["wqT"], ops[1]["sw"], None)]
+    wgt = [(B.OP_WGRAD, o["dyTq"], o["sdyT"], o["xTq"], o["sxT"], None) for o in ops]
+    got_fwd = B.fp8bs_gemm_group(fwd)
+    got_wgt = B.fp8bs_gemm_group(wgt)
+    assert B.fp8bs_get_device_status() == 0
+    single_fwd = [B.fp8bs_gemm_fprop(o["xq"], o["sx"], o["wq"], o["sw"], split=False) for o in ops] + \
+                 [B.fp8bs_gemm_dgrad(ops[1]["dyq"], ops[1]["sdy"], ops[1]["wqT"], ops[1]["sw"], split=False)]
+    single_wgt = [B.fp8bs_gemm_wgrad(o["dyTq"], o["sdyT"], o["xTq"], o["sxT"], split=False) for o in ops]
+    assert B.fp8bs_get_device_status() == 0
+    for g, s1 in zip(got_fwd + got_wgt, single_fwd + single_wgt):
+        assert torch.equal(g.view(torch.int16), s1.view(torch.int16))
+    o = ops[0]
+    oxq, osx = oracle.quant_rowwise_1x128(o["x"])
+    owq, _, osw = oracle.quant_weight_128x128(o["w"], want_t=False)
+    acc, _, sab = oracle_gemm_rows("fprop", oxq, osx, owq, osw, np.arange(300))
+    assert_gemm_close(np_bf16_bits(got_fwd[0]), acc, sab, "grouped fprop")
+    oxTq, osxT = oracle.quant_colwise_128x1_T(o["x"])
+    odyTq, osdyT = oracle.quant_colwise_128x1_T(o["dy"])
+    acc, _, sab = oracle_gemm_rows("wgrad", odyTq, osdyT, oxTq, osxT, np.arange(384))
+    assert_gemm_close(np_bf16_bits(got_wgt[0]), acc, sab, "grouped wgrad")
+
+
 @pytest.mark.parametrize("M,N,K", [(384, 256, 640), (8192, 2048, 5632)])
 def test_wgrad_accumulates_in_fp32(M, N, K):
     """dW (FP32) += dY^T X, twice, starting from random FP32 values: every
