@@ -237,6 +237,16 @@ def sweep(peaks, fp8_peak):
             l.run()
         torch.cuda.synchronize()
         out = {}
+        from fp8_block_scaled_16_b300 import binding as B
+        from fp8_block_scaled_16_b300.linear import Launch
+
+        # The forward product with its FP8 1x128 output quantized in the epilogue
+        # (no BF16 output): what a following linear would consume.
+        yq = torch.empty(lin.tokens, lin.out_features, dtype=torch.uint8, device="cuda")
+        sy = torch.empty(lin.out_features // 128, B.padded_tokens(lin.tokens), dtype=torch.float32, device="cuda")
+        ll = ll + [Launch("fprop_fp8_out", 2 * lin.tokens * lin.out_features * lin.in_features, "flops",
+                          lambda: B.fp8bs_gemm_fprop_quant(st.xq, st.sx, st.wq, st.sw, want_bf16=False, yq=yq,
+                                                           sy=sy))]
         for i, l in enumerate(ll):
             times = []
             for _ in range(10):
@@ -256,7 +266,7 @@ def sweep(peaks, fp8_peak):
                 gbs = l.work / (ms * 1e-3) / 1e9
                 out[key] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)}
         res[name] = out
-        del st, d, ll
+        del st, d, ll, yq, sy
         torch.cuda.empty_cache()
     return res
 

@@ -45,6 +45,7 @@ SIGNATURES = {
     "fp8bs_quantize_weight": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
     "fp8bs_gemm_fprop": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_gemm_dgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8bs_gemm_fprop_quant": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_gemm_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_get_device_status": (ctypes.c_int, [_P]),
     "fp8bs_set_workspace": (ctypes.c_int, [_P, _I64]),
@@ -186,6 +187,26 @@ def fp8bs_gemm_fprop(xq, sx, wq, sw, y=None, stream=None, split=True) -> torch.T
         _dev(wq, torch.uint8, (N, K), "wq"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
         _dev(y, torch.bfloat16, (M, N), "y"), M, N, K, _stream(stream)), "fp8bs_gemm_fprop")
     return y
+
+
+def fp8bs_gemm_fprop_quant(xq, sx, wq, sw, y=None, yq=None, sy=None, want_bf16=True, stream=None, split=True):
+    """Y = X W^T with Y's 1x128 row-wise quantization done in the GEMM's
+    epilogue.  Returns (y or None, yq u8 [M][N], sy f32 [N/128][Mp]); yq/sy
+    equal fp8bs_quantize_act(y, ROWWISE)."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    if split:
+        _ensure_workspace(OP_FPROP, M, N, K, xq.device)
+    y = _out(y, (M, N), torch.bfloat16, xq.device) if want_bf16 else None
+    yq = _out(yq, (M, N), torch.uint8, xq.device)
+    sy = _out(sy, (N // 128, padded_tokens(M)), torch.float32, xq.device)
+    _check(load().fp8bs_gemm_fprop_quant(
+        _dev(xq, torch.uint8, (M, K), "xq"), _dev(sx, torch.float32, (K // 128, padded_tokens(M)), "sx"),
+        _dev(wq, torch.uint8, (N, K), "wq"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
+        _dev(y, torch.bfloat16, (M, N), "y") if y is not None else None,
+        _dev(yq, torch.uint8, (M, N), "yq"), _dev(sy, torch.float32, (N // 128, padded_tokens(M)), "sy"),
+        M, N, K, _stream(stream)), "fp8bs_gemm_fprop_quant")
+    return y, yq, sy
 
 
 def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None, split=True) -> torch.Tensor:

@@ -193,8 +193,10 @@ struct GemmSpec {
     const float* sa;
     const float* sb;
     int64_t sb_stride_j, sb_stride_b;
-    void* out;
+    void* out;             // BF16 (or FP32 with out_f32_add); may be null when out_q is set
     bool out_f32_add;
+    uint8_t* out_q = nullptr;  // forward only: 1x128-quantized output and its scales
+    float* out_s = nullptr;
 };
 
 // The operand roles of product `op` called with its entry point's arguments.
@@ -221,17 +223,26 @@ GemmSpec spec_of(int op, const uint8_t* a, const float* sa, const uint8_t* b, co
 
 // Tensor maps and kernel parameters of one product, not split.
 int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmC,
-                gemm::Params* p) {
+                CUtensorMap* tmQ, gemm::Params* p) {
     using namespace gemm;
     constexpr int BN = 256;
+    // Without a BF16 output the store map is encoded on the FP8 payload and never used.
+    const void* cbase = s.out != nullptr ? s.out : static_cast<const void*>(s.out_q);
     if (!tmap_2d(tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.A, s.kc, s.rows, s.kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tmap_2d(tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.B, s.kc, s.cols, s.kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !(s.out_f32_add ? tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, s.out, s.cols, s.rows, s.cols * 4, 32, 32,
+        !(s.out_f32_add ? tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cbase, s.cols, s.rows, s.cols * 4, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_128B)
-                        : tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.out, s.cols, s.rows, s.cols * 2, 64, 32,
+                        : tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cbase, s.cols, s.rows, s.cols * 2, 64, 32,
                                   CU_TENSOR_MAP_SWIZZLE_128B)))
         return FP8BS_ERR_LAUNCH;
+    if (s.out_q != nullptr &&
+        !tmap_2d(tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.out_q, s.cols, s.rows, s.cols, 128, 32,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8BS_ERR_LAUNCH;
     p->out_f32_add = s.out_f32_add ? 1 : 0;
+    p->out_bf16 = s.out != nullptr ? 1 : 0;
+    p->out_q = s.out_q != nullptr ? 1 : 0;
+    p->out_s = s.out_s;
     p->m_tiles = static_cast<int32_t>((s.rows + BM - 1) / BM);
     p->sa_ld = padded_tokens(s.rows);
     p->n_tiles = static_cast<int32_t>((s.cols + BN - 1) / BN);
@@ -283,7 +294,7 @@ int run_gemm(const GemmSpec& s, cudaStream_t st) {
     if (rc != FP8BS_OK) return rc;
     Group<1> grp;
     Params& p = grp.p[0];
-    rc = fill_member(d, s, &grp.tmA[0], &grp.tmB[0], &grp.tmC[0], &p);
+    rc = fill_member(d, s, &grp.tmA[0], &grp.tmB[0], &grp.tmC[0], &grp.tmQ[0], &p);
     if (rc != FP8BS_OK) return rc;
     p.fault = g_fault.exchange(0);
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -366,6 +377,18 @@ int fp8bs_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, cons
     return run_gemm(spec_of(FP8BS_OP_FPROP, xq, sx, wq, sw, y, M, N, K), static_cast<cudaStream_t>(stream));
 }
 
+int fp8bs_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, void* y,
+                           uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K, void* stream) {
+    int rc = check_gemm_args(xq, sx, wq, sw, yq, M, N, K);
+    if (rc != FP8BS_OK) return rc;
+    if (sy == nullptr) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(sy) || (y != nullptr && !aligned16(y))) return FP8BS_ERR_ALIGN;
+    GemmSpec s = spec_of(FP8BS_OP_FPROP, xq, sx, wq, sw, y, M, N, K);
+    s.out_q = yq;
+    s.out_s = sy;
+    return run_gemm(s, static_cast<cudaStream_t>(stream));
+}
+
 int fp8bs_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw, void* dx,
                      int64_t M, int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(dyq, sdy, wqT, sw, dx, M, N, K);
@@ -412,7 +435,7 @@ int fp8bs_gemm_group(const fp8bs_gemm_args* gemms, int count, void* stream) {
     for (int i = 0; i < count; i++) {
         const fp8bs_gemm_args& a = gemms[i];
         rc = fill_member(d, spec_of(a.op, a.a, a.sa, a.b, a.sb, a.out, a.M, a.N, a.K), &grp.tmA[i], &grp.tmB[i],
-                         &grp.tmC[i], &grp.p[i]);
+                         &grp.tmC[i], &grp.tmQ[i], &grp.p[i]);
         if (rc != FP8BS_OK) return rc;
         const int64_t end = grp.first_unit[i] + static_cast<int64_t>(grp.p[i].m_tiles) * grp.p[i].n_tiles;
         if (end > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
@@ -498,7 +521,7 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
     Group<1> grp;
     Params& p = grp.p[0];
     rc = fill_member(d, spec_of(FP8BS_OP_WGRAD, dyTq, sdyT, xTq, sxT, dw, M, N, K), &grp.tmA[0], &grp.tmB[0],
-                     &grp.tmC[0], &p);
+                     &grp.tmC[0], &grp.tmQ[0], &p);
     if (rc != FP8BS_OK) return rc;
     if (sp.splits > 1) {
         // The scratch keeps whatever the previous call left: clear the flags

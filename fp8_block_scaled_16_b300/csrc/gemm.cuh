@@ -132,6 +132,12 @@ struct Params {
     uint64_t timeout_ns;
     int32_t fault;                // test hook: withhold CTA 0's first operand copy
     int32_t out_f32_add;          // 0: BF16 store into out; 1: FP32 out += result (tmC is FP32)
+    int32_t out_bf16;             // store the BF16 output (tmC); 0 only with out_q
+    // Forward product only: the BF16-rounded output also quantized in 1x128
+    // row tiles -- E4M3 payload [rows][cols] through tmQ, FP32 scales
+    // out_s[cols/128][sa_ld] (null: not requested).
+    float* out_s;
+    int32_t out_q;
     // K splits (1 = none) of the tiles t >= tail_first (0: of every tile).
     // With T = tiles - tail_first split tiles, split s > 0 of tile t is a
     // helper that leaves its FP32 partial in ws slot (s-1)*T + (t-tail_first)
@@ -188,7 +194,7 @@ __device__ __forceinline__ Unit unit_of(int u, const Params& p, int num_tiles) {
 constexpr int kGroupMax = 4;
 template <int G>
 struct Group {
-    CUtensorMap tmA[G], tmB[G], tmC[G];
+    CUtensorMap tmA[G], tmB[G], tmC[G], tmQ[G];
     Params p[G];
     int32_t count;
     int32_t first_unit[G + 1];
@@ -341,6 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             tma_prefetch_desc(&grp.tmA[g]);
             tma_prefetch_desc(&grp.tmB[g]);
             tma_prefetch_desc(&grp.tmC[g]);
+            if (grp.p[g].out_q) tma_prefetch_desc(&grp.tmQ[g]);
         }
     }
     if (warp == 1) {
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                         bulk_commit_group();
                     }
                 }
-            } else if (jvalid && rvalid) {
+            } else if (jvalid && rvalid && p.out_bf16) {
                 // BF16 out through shared memory and two TMA stores (32 rows x 64
                 // columns each) per warp.  The 128-byte swizzle puts the 16-byte
                 // chunk c of row r at chunk c ^ (r % 8), so the 32 lanes' row
@@ -717,6 +724,51 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                     tma_store_2d(&grp.tmC[g], stage_out, x0, y0);
                     tma_store_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, x0 + 64, y0);
                     bulk_commit_group();
+                }
+            }
+            if constexpr (SBMODE == SB_SCALAR) {
+                if (p.out_q && jvalid) {
+                    // FP8 output for the next linear: this thread holds one row's 128
+                    // columns, i.e. one whole 1x128 tile.  Round to BF16 (the value the
+                    // BF16 output holds), amax, the scheme's scale, E4M3 cast -- the
+                    // operations of the row-wise quantizer on that BF16 row.
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < COLS; j += 2) {
+                        const uint32_t w2 = f32x2_to_bf16x2(acc[j], acc[j + 1]);
+                        acc[j] = bf16lo_to_f32(w2);
+                        acc[j + 1] = bf16hi_to_f32(w2);
+                        amax = fmaxf(amax, fmaxf(fabsf(acc[j]), fabsf(acc[j + 1])));
+                    }
+                    float sq, inv;
+                    tile_scale(amax, sq, inv);
+                    // Scales of every row of the tile, padding rows (all-zero, s = 1) included.
+                    p.out_s[static_cast<int64_t>(jb) * p.sa_ld + static_cast<int64_t>(mb) * BM + row] = sq;
+                    if (rvalid) {
+                        const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
+                        if (lane == 0) bulk_wait_read_all();  // earlier stores have read the buffer
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 8; c++) {
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int q = 0; q < 4; q++) {
+                                const int j = c * 16 + q * 4;
+                                wv[q] = e4m3x2(__fmul_rn(acc[j], inv), __fmul_rn(acc[j + 1], inv)) |
+                                        (e4m3x2(__fmul_rn(acc[j + 2], inv), __fmul_rn(acc[j + 3], inv)) << 16);
+                            }
+                            const uint32_t a = stage_out + static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4));
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]),
+                                         "r"(wv[2]), "r"(wv[3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&grp.tmQ[g], stage_out, nb * BN + half * COLS, mb * BM + quad * 32);
+                            bulk_commit_group();
+                        }
+                    }
                 }
             }
         }

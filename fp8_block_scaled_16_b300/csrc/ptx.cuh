@@ -3,6 +3,7 @@
 // conversion, and bounded waits that give up instead of hanging.
 #pragma once
 
+#include <cfloat>
 #include <cstdint>
 #include <cuda.h>
 
@@ -270,6 +271,20 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Tile scale of the scheme: s = amax/448 and inv = 448/amax, both IEEE
+// round-to-nearest; an all-zero tile gets s = inv = 1; an overflowing inv is
+// clamped to FLT_MAX.  Shared by the quantizers and the GEMM's FP8 epilogue,
+// so both encode a tile identically.
+__device__ __forceinline__ void tile_scale(float amax, float& s, float& inv) {
+    if (amax == 0.0f) {
+        s = 1.0f;
+        inv = 1.0f;
+        return;
+    }
+    s = __fdiv_rn(amax, 448.0f);
+    inv = fminf(__fdiv_rn(448.0f, amax), FLT_MAX);
 }
 
 // Per-halfword unsigned max of two packed pairs.

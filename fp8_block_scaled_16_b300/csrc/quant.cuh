@@ -27,18 +27,6 @@ namespace fp8bs {
 
 enum : int { QM_ROW = 1, QM_COLT = 2, QM_BLOCK = 4 };
 
-// s = amax/448 and inv = 448/amax, both IEEE round-to-nearest; an all-zero
-// tile gets s = inv = 1; an overflowing inv is clamped to FLT_MAX.
-__device__ __forceinline__ void tile_scale(float amax, float& s, float& inv) {
-    if (amax == 0.0f) {
-        s = 1.0f;
-        inv = 1.0f;
-        return;
-    }
-    s = __fdiv_rn(amax, 448.0f);
-    inv = fminf(__fdiv_rn(448.0f, amax), FLT_MAX);
-}
-
 // Four E4M3 codes from the low (lo = true) or high BF16 halves of four words.
 __device__ __forceinline__ uint32_t e4m3x4_half(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, float iv,
                                                 bool lo) {

@@ -121,6 +121,24 @@ int fp8bs_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, cons
                      void* y, int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * Forward GEMM with an FP8 output for the next linear:  Y = X W^T, then Y's
+ * 1x128 row-wise quantization, in the GEMM's epilogue (no extra pass over Y).
+ *   xq, sx, wq, sw, M, N, K : as for fp8bs_gemm_fprop.
+ *   y  : BF16 [M][N] output, or NULL to skip it.
+ *   yq : E4M3 [M][N] and sy : FP32 [N/128][Mp] (Mp = M rounded up to 128;
+ *        padding rows get s = 1) -- exactly what fp8bs_quantize_act with
+ *        FP8BS_ROWWISE writes for the BF16 Y: each 1x128 tile of the
+ *        BF16-rounded product gets s = amax/448 and E4M3(y * 448/amax).
+ * The weight gradient of the next linear still needs Y's 128x1 transposed
+ * quantization (fp8bs_quantize_act with FP8BS_COLWISE_T on the BF16 Y).
+ * Passage: the pages keep the FP8 path on the main linear GEMMs and their
+ * inputs (blog section "FP8：加快 RTX 5090 上的训练"); this fuses the
+ * quantization of a linear's FP8 input into the producing GEMM.
+ */
+int fp8bs_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, void* y,
+                           uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * Data-gradient GEMM  dX = dY W  (BF16 out [M][K]); contraction over N.
  *   dyq [M][N] E4M3 with sdy [N/128][Mp] (fp8bs_quantize_act on dY, ROWWISE),
  *   wqT [K][N] E4M3 (the transposed payload from fp8bs_quantize_weight),

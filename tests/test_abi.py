@@ -76,6 +76,13 @@ def test_validation_before_launch(lib):
         assert fn(fake, fake, fake, fake, fake, -5, 256, 128, None) == 2
         assert fn(fake, fake, fake, fake, fake, 128, 200, 128, None) == 2
         assert fn(fake, fake, fake, odd, fake, 128, 128, 128, None) == 3
+    fq = lib.fp8bs_gemm_fprop_quant
+    assert fq(fake, fake, fake, fake, None, fake, None, 128, 256, 128, None) == 1      # no scales for Yq
+    assert fq(fake, fake, fake, fake, None, None, fake, 128, 256, 128, None) == 1      # no Yq
+    assert fq(fake, fake, fake, fake, None, fake, fake, 128, 200, 128, None) == 2
+    assert fq(fake, fake, fake, fake, None, odd, fake, 128, 256, 128, None) == 3
+    assert fq(fake, fake, fake, fake, odd, fake, fake, 128, 256, 128, None) == 3       # optional Y misaligned
+    assert fq(fake, fake, fake, fake, None, fake, odd, 128, 256, 128, None) == 3
     assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, None, None) == 1
     assert lib.fp8bs_debug_e4m3_encode_bits(0xFFFFFFF0, 32, fake, None) == 2
     assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, odd, None) == 3

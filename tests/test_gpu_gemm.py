@@ -269,6 +269,49 @@ def test_grouped_launch_equals_single_launches():
     assert_gemm_close(np_bf16_bits(got_wgt[0]), acc, sab, "grouped wgrad")
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (300, 384, 640),      # token tail, ragged last column tile
+    (2432, 2048, 4096),   # the last wave's tiles split in 4 (owners quantize after the fix-up)
+    (8192, 3072, 2048),   # attention QKV forward at 8192 tokens
+])
+def test_fprop_with_fp8_output(M, N, K):
+    """fp8bs_gemm_fprop_quant quantizes Y in the GEMM's epilogue.  Its BF16 Y
+    equals fp8bs_gemm_fprop's bitwise; its E4M3 payload and scales equal the
+    row-wise quantizer's on that BF16 Y bit for bit (the quantizer is pinned
+    bit-exactly to the oracle by the quantizer tests), also when no BF16 Y is
+    written; and the dequantized payload stays within the oracle product's
+    tolerance plus one E4M3 rounding (|e| <= 2^-4 |v| above 2^-6 of the tile
+    scale, <= 2^-10 of it below) on every output row of the first shape and
+    on the last 128 rows (the split tiles of the second) + 64 seeded others
+    of the larger two."""
+    x = inputs.random_bf16((M, K), seed=7 + M)
+    w = inputs.random_bf16((N, K), seed=8 + N, std=0.02)
+    xq, sx, _, _ = B.fp8bs_quantize_act(x.cuda(), B.ROWWISE)
+    wq, _, sw = B.fp8bs_quantize_weight(w.cuda(), want_t=False)
+    y_plain = B.fp8bs_gemm_fprop(xq, sx, wq, sw)
+    y, yq, sy = B.fp8bs_gemm_fprop_quant(xq, sx, wq, sw)
+    _, yq2, sy2 = B.fp8bs_gemm_fprop_quant(xq, sx, wq, sw, want_bf16=False)
+    assert B.fp8bs_get_device_status() == 0
+    assert torch.equal(y.view(torch.int16), y_plain.view(torch.int16))
+    q_ref, s_ref, _, _ = B.fp8bs_quantize_act(y, B.ROWWISE)
+    assert torch.equal(yq, q_ref)
+    assert torch.equal(sy.view(torch.int32), s_ref.view(torch.int32))
+    assert torch.equal(yq2, yq) and torch.equal(sy2.view(torch.int32), sy.view(torch.int32))
+
+    rows = np.arange(M) if M * N * K < 2 ** 34 else \
+        np.concatenate([inputs.sample_rows(M - 128, 4343, 64).numpy(), np.arange(M - 128, M)])
+    oxq, osx = oracle.quant_rowwise_1x128(x)
+    owq, _, osw = oracle.quant_weight_128x128(w, want_t=False)
+    acc, _, sab = oracle_gemm_rows("fprop", oxq, osx, owq, osw, rows)
+    s_rows = np_f32(sy)[:, rows].T                                  # [rows][N/128]
+    scale = np.repeat(s_rows, 128, axis=1).astype(np.float64)       # per element
+    deq = oracle.e4m3_decode(np_u8(yq)[rows]) * scale
+    ref = acc.astype(np.float64)
+    gemm_tol = 2.0 ** -8 * np.abs(ref) + 1e-6 * sab
+    bound = gemm_tol + 2.0 ** -4 * (np.abs(ref) + gemm_tol) + 2.0 ** -10 * scale
+    assert np.all(np.abs(deq - ref) <= bound), float(np.max(np.abs(deq - ref) - bound))
+
+
 @pytest.mark.parametrize("M,N,K", [(384, 256, 640), (8192, 2048, 5632)])
 def test_wgrad_accumulates_in_fp32(M, N, K):
     """dW (FP32) += dY^T X, twice, starting from random FP32 values: every
