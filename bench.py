@@ -384,16 +384,22 @@ def summarize_kernels(per):
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources; a stored ncu traffic figure is only used
-    while the kernels it was measured on are unchanged."""
+    """Hash of the CUDA sources' code (comments and blank lines removed); a
+    stored ncu traffic figure is only used while the kernels it was measured
+    on are unchanged."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_16_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", "", text)
+            code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+            h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -20,27 +20,31 @@
 //       accumulate off, then commits to free the smem stage and to publish
 //       the buffer;
 //   warp 2: scale loader -- per K block the 128 row scales (and, for the
-//       weight gradient, the 256 column scales) into an 8-slot shared-memory
-//       ring with cp.async, one 16-byte copy per lane;
+//       weight gradient, the 256 column scales, regrouped for the epilogue's
+//       layout) into an 8-slot shared-memory ring with cp.async;
 //   warp 3: idle (it completes the first warpgroup, whose registers are
 //       handed to the epilogue warpgroups with setmaxnreg);
 //   warps 4..11: promotion + epilogue -- each warp owns a 32-lane TMEM
 //       quadrant (rows) and one 128-column half; per K block it loads its
-//       partial with tcgen05.ld two 32-column chunks at a time, releases the
-//       TMEM buffer after the last load, and does acc = fma(P_b, sa*sb, acc)
-//       with packed FP32 FMAs on 128 registers per thread; at the end of a
-//       tile it writes the result through swizzled shared staging and TMA
-//       (BF16 stores, or FP32 reduce-adds for an accumulating weight
-//       gradient).
+//       partial with tcgen05.ld, 64 columns at a time (.32x32b: a row per
+//       thread; the weight gradient uses .16x256b: 4 rows x 32 columns per
+//       thread, fewer column scales to load), releases the TMEM buffer after
+//       the last load, and does acc = fma(P_b, sa*sb, acc) with packed FP32
+//       FMAs on 128 registers per thread; at the end of a tile it writes the
+//       result through swizzled shared staging and TMA: BF16 stores, FP32
+//       reduce-adds for an accumulating weight gradient, and/or, for a
+//       forward product, the output's 1x128 E4M3 quantization (a thread's
+//       128 columns are one whole tile).
 // While the epilogue promotes block b, the tensor cores already compute
 // block b+1 into the other buffer.
 //
 // Work comes in units (tile, K range): one per tile, or, where the last wave
 // of tiles would leave many SMs idle, 2-8 splits of the contraction of some
 // or all tiles, whose FP32 partials meet in caller-provided scratch (see
-// Params::splits).  Rows past
-// the output's last row (a token count that is not a multiple of 128) read
-// zeros through TMA and are not stored.
+// Params::splits).  One launch may compute several products (Group): their
+// units are dealt to the persistent CTAs as one list.  Rows past the
+// output's last row (a token count that is not a multiple of 128) read zeros
+// through TMA and are not stored.
 //
 // The scale ring is written with cp.async (generic proxy) rather than TMA:
 // the epilogue reads it with ordinary loads, and a TMA write into a slot
