@@ -19,7 +19,10 @@ Pinned by ``tests/test_oracle_*.py`` (CPU only):
     error bound, the all-zero tile);
   * GEMMs: integer brute force of one 128^3 block, a float64 GEMM of the
     dequantized operands within the analytic promotion bound, the unit-scale
-    special case, and the fprop/dgrad/wgrad transposition identities.
+    special case, and the fprop/dgrad/wgrad transposition identities;
+  * SwiGLU activation (tests/test_oracle_activation.py): its exponential
+    within 1 ulp of float64 e^x, SiLU(g)*u within one BF16 ulp of the
+    float64 formula on every BF16 g in [-24, 24], and its special cases.
 """
 from __future__ import annotations
 
@@ -66,6 +69,10 @@ _SIGS = {
     "orc_e4m3_encode_array": (None, [_P, _I, _P]),
     "orc_e4m3_encode_bits": (None, [ctypes.c_uint32, _I, _P]),
     "orc_e4m3_decode_array": (None, [_P, _I, _P]),
+    "orc_exp_cw": (ctypes.c_float, [ctypes.c_float]),
+    "orc_silu_mul_bf16": (ctypes.c_uint16, [ctypes.c_uint16, ctypes.c_uint16]),
+    "orc_silu_mul_array": (None, [_P, _P, _I, _P]),
+    "orc_exp_cw_array": (None, [_P, _I, _P]),
 }
 
 
@@ -219,3 +226,23 @@ def gemm_wgrad(dytq, sdyt, xtq, sxt, rows=None):
     K = xtq.shape[0]
     return _gemm(lib().orc_gemm_wgrad, dytq, sdyt, xtq, sxt, M, N, K, rows, K, N)
 
+
+
+# ---------------------------------------------------------------- activation
+
+def exp_cw(x: np.ndarray) -> np.ndarray:
+    """e^x in FP32 by Cody-Waite reduction and a degree-7 Taylor polynomial."""
+    v = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(v.shape, np.float32)
+    lib().orc_exp_cw_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def silu_mul(g, u) -> np.ndarray:
+    """h = SiLU(g) * u elementwise on BF16 bit patterns (uint16 arrays or
+    bf16 tensors of one shape); returns BF16 bits."""
+    gb, ub = _bf16_bits(g), _bf16_bits(u)
+    assert gb.shape == ub.shape
+    out = np.empty(gb.shape, np.uint16)
+    lib().orc_silu_mul_array(_ptr(gb), _ptr(ub), gb.size, _ptr(out))
+    return out

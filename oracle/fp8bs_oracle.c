@@ -376,3 +376,63 @@ void orc_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out) {
 void orc_e4m3_decode_array(const uint8_t* c, int64_t n, double* out) {
     for (int64_t i = 0; i < n; i++) out[i] = orc_e4m3_decode(c[i]);
 }
+
+/* ------------------------------------------------------------------ */
+/* SwiGLU activation between the gate+up and down projections          */
+/* ------------------------------------------------------------------ */
+
+/* e^x in FP32 by the Cody-Waite method (W. J. Cody and W. Waite, "Software
+ * Manual for the Elementary Functions", 1980): x = n ln2 + r with
+ * n = rint(x log2 e) and r computed with a two-part ln 2 (the high part
+ * has 16 significant bits, so n * LN2_HI is exact for |n| < 256), then
+ * e^r by its Taylor polynomial of degree 7 (|r| <= ln2/2, remainder below
+ * 2^-27 relative), then the factor 2^n.  Every step is one IEEE FP32
+ * operation in the order written (fmaf where written, no contraction).
+ * Reading (range): x > 88 gives +Inf and x < -87 gives 0, so 2^n stays a
+ * normal power of two; the activation's inputs lie far inside. */
+static const float LOG2E_F = 1.44269502f;          /* log2(e) rounded to FP32 */
+static const float LN2_HI_F = 0.693145751953125f;  /* 45426 / 2^16 */
+static const float LN2_LO_F = 1.42860677e-06f;     /* ln 2 - LN2_HI, rounded */
+
+float orc_exp_cw(float x) {
+    if (x > 88.0f) return INFINITY;
+    if (x < -87.0f) return 0.0f;
+    float n = rintf(x * LOG2E_F);
+    float r = fmaf(-n, LN2_HI_F, x);
+    r = fmaf(-n, LN2_LO_F, r);
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    uint32_t bits = (uint32_t)((int32_t)n + 127) << 23; /* 2^n, n in [-126, 127] */
+    float two_n;
+    memcpy(&two_n, &bits, 4);
+    return p * two_n;
+}
+
+/* h = SiLU(g) * u of one element, SiLU(g) = g / (1 + e^-g): g and u are
+ * the BF16 outputs of the gate and up projections (what a BF16 forward
+ * product holds); the activation runs in FP32 and h is rounded to BF16.
+ * Reading: the pages keep the activation out of the FP8 path and give no
+ * formula; this is the SwiGLU form, g * sigmoid(g) * u, evaluated as
+ * g / (1 + e^-g) * u with one rounding per operation. */
+uint16_t orc_silu_mul_bf16(uint16_t g_bits, uint16_t u_bits) {
+    float g = orc_bf16_to_f32(g_bits);
+    float u = orc_bf16_to_f32(u_bits);
+    float t = orc_exp_cw(-g);
+    float d = 1.0f + t;
+    float sg = g / d;
+    return orc_f32_to_bf16(sg * u);
+}
+
+void orc_silu_mul_array(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h) {
+    for (int64_t i = 0; i < n; i++) h[i] = orc_silu_mul_bf16(g[i], u[i]);
+}
+
+void orc_exp_cw_array(const float* x, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; i++) out[i] = orc_exp_cw(x[i]);
+}
