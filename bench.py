@@ -247,6 +247,16 @@ def sweep(peaks, fp8_peak):
         ll = ll + [Launch("fprop_fp8_out", 2 * lin.tokens * lin.out_features * lin.in_features, "flops",
                           lambda: B.fp8bs_gemm_fprop_quant(st.xq, st.sx, st.wq, st.sw, want_bf16=False, yq=yq,
                                                            sy=sy))]
+        if name.startswith("mlp_gate_up"):
+            # The gate+up forward with SiLU(gate) * up and the down projection's
+            # FP8 input in the epilogue (the weight's rows taken as interleaved
+            # gate/up blocks; the timing does not depend on the values).
+            I = lin.out_features // 2
+            hq = torch.empty(lin.tokens, I, dtype=torch.uint8, device="cuda")
+            sh = torch.empty(I // 128, B.padded_tokens(lin.tokens), dtype=torch.float32, device="cuda")
+            ll.append(Launch("fprop_swiglu_fp8_out", 2 * lin.tokens * lin.out_features * lin.in_features, "flops",
+                             lambda: B.fp8bs_gemm_fprop_swiglu_quant(st.xq, st.sx, st.wq, st.sw, want_bf16=False,
+                                                                     hq=hq, sh=sh)))
         for i, l in enumerate(ll):
             times = []
             for _ in range(10):

@@ -13,7 +13,7 @@ import importlib
 _BINDING_NAMES = (
     "ROWWISE", "COLWISE_T", "Fp8bsError",
     "fp8bs_quantize_act", "fp8bs_quantize_weight", "fp8bs_gemm_fprop", "fp8bs_gemm_dgrad",
-    "fp8bs_gemm_fprop_quant",
+    "fp8bs_gemm_fprop_quant", "fp8bs_gemm_fprop_swiglu_quant", "fp8bs_debug_silu_mul",
     "fp8bs_gemm_wgrad", "fp8bs_get_device_status", "fp8bs_status_string", "fp8bs_launch_count",
     "fp8bs_debug_set_wait_timeout_ns", "fp8bs_debug_set_fault", "fp8bs_debug_e4m3_encode_bits",
     "fp8bs_debug_split_plan",

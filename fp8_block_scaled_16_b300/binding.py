@@ -46,6 +46,8 @@ SIGNATURES = {
     "fp8bs_gemm_fprop": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_gemm_dgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_gemm_fprop_quant": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8bs_gemm_fprop_swiglu_quant": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8bs_debug_silu_mul": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
     "fp8bs_gemm_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_get_device_status": (ctypes.c_int, [_P]),
     "fp8bs_set_workspace": (ctypes.c_int, [_P, _I64]),
@@ -207,6 +209,38 @@ def fp8bs_gemm_fprop_quant(xq, sx, wq, sw, y=None, yq=None, sy=None, want_bf16=T
         _dev(yq, torch.uint8, (M, N), "yq"), _dev(sy, torch.float32, (N // 128, padded_tokens(M)), "sy"),
         M, N, K, _stream(stream)), "fp8bs_gemm_fprop_quant")
     return y, yq, sy
+
+
+def fp8bs_gemm_fprop_swiglu_quant(xq, sx, wq, sw, h=None, hq=None, sh=None, want_bf16=True, stream=None,
+                                  split=True):
+    """H = SiLU(X Wg^T) * (X Wu^T) from the gate+up weight interleaved in
+    128-row blocks (see interleave_gate_up in linear.py), with H's 1x128
+    quantization.  Returns (h or None, hq u8 [M][I], sh f32 [I/128][Mp])."""
+    M, K = xq.shape
+    N2 = wq.shape[0]
+    I = N2 // 2
+    if split:
+        _ensure_workspace(OP_FPROP, M, N2, K, xq.device)
+    h = _out(h, (M, I), torch.bfloat16, xq.device) if want_bf16 else None
+    hq = _out(hq, (M, I), torch.uint8, xq.device)
+    sh = _out(sh, (I // 128, padded_tokens(M)), torch.float32, xq.device)
+    _check(load().fp8bs_gemm_fprop_swiglu_quant(
+        _dev(xq, torch.uint8, (M, K), "xq"), _dev(sx, torch.float32, (K // 128, padded_tokens(M)), "sx"),
+        _dev(wq, torch.uint8, (N2, K), "wq"), _dev(sw, torch.float32, (N2 // 128, K // 128), "sw"),
+        _dev(h, torch.bfloat16, (M, I), "h") if h is not None else None,
+        _dev(hq, torch.uint8, (M, I), "hq"), _dev(sh, torch.float32, (I // 128, padded_tokens(M)), "sh"),
+        M, N2, K, _stream(stream)), "fp8bs_gemm_fprop_swiglu_quant")
+    return h, hq, sh
+
+
+def fp8bs_debug_silu_mul(g: torch.Tensor, u: torch.Tensor, h=None, stream=None) -> torch.Tensor:
+    """h = bf16(SiLU(g) * u) elementwise for BF16 CUDA tensors of one shape."""
+    h = _out(h, tuple(g.shape), torch.bfloat16, g.device)
+    _dev(u, torch.bfloat16, tuple(g.shape), "u")
+    _check(load().fp8bs_debug_silu_mul(_dev(g, torch.bfloat16, tuple(g.shape), "g"), u.data_ptr(), g.numel(),
+                                       _dev(h, torch.bfloat16, tuple(g.shape), "h"), _stream(stream)),
+           "fp8bs_debug_silu_mul")
+    return h
 
 
 def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None, split=True) -> torch.Tensor:

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "fp8bs.h"
+#include "act.cuh"
 #include "gemm.cuh"
 #include "quant.cuh"
 
@@ -197,6 +198,7 @@ struct GemmSpec {
     bool out_f32_add;
     uint8_t* out_q = nullptr;  // forward only: 1x128-quantized output and its scales
     float* out_s = nullptr;
+    bool swiglu = false;       // forward of an interleaved gate+up weight: outputs are H = SiLU(gate) * up
 };
 
 // The operand roles of product `op` called with its entry point's arguments.
@@ -228,17 +230,19 @@ int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap*
     constexpr int BN = 256;
     // Without a BF16 output the store map is encoded on the FP8 payload and never used.
     const void* cbase = s.out != nullptr ? s.out : static_cast<const void*>(s.out_q);
+    const int64_t ocols = s.swiglu ? s.cols / 2 : s.cols;  // columns of the stored output
     if (!tmap_2d(tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.A, s.kc, s.rows, s.kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tmap_2d(tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.B, s.kc, s.cols, s.kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !(s.out_f32_add ? tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cbase, s.cols, s.rows, s.cols * 4, 32, 32,
+        !(s.out_f32_add ? tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cbase, ocols, s.rows, ocols * 4, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_128B)
-                        : tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cbase, s.cols, s.rows, s.cols * 2, 64, 32,
+                        : tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cbase, ocols, s.rows, ocols * 2, 64, 32,
                                   CU_TENSOR_MAP_SWIZZLE_128B)))
         return FP8BS_ERR_LAUNCH;
     if (s.out_q != nullptr &&
-        !tmap_2d(tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.out_q, s.cols, s.rows, s.cols, 128, 32,
+        !tmap_2d(tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.out_q, ocols, s.rows, ocols, 128, 32,
                  CU_TENSOR_MAP_SWIZZLE_128B))
         return FP8BS_ERR_LAUNCH;
+    p->out_swiglu = s.swiglu ? 1 : 0;
     p->out_f32_add = s.out_f32_add ? 1 : 0;
     p->out_bf16 = s.out != nullptr ? 1 : 0;
     p->out_q = s.out_q != nullptr ? 1 : 0;
@@ -386,6 +390,20 @@ int fp8bs_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq
     GemmSpec s = spec_of(FP8BS_OP_FPROP, xq, sx, wq, sw, y, M, N, K);
     s.out_q = yq;
     s.out_s = sy;
+    return run_gemm(s, static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_gemm_fprop_swiglu_quant(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, void* h,
+                                  uint8_t* hq, float* sh, int64_t M, int64_t N2, int64_t K, void* stream) {
+    int rc = check_gemm_args(xq, sx, wq, sw, hq, M, N2, K);
+    if (rc != FP8BS_OK) return rc;
+    if (sh == nullptr) return FP8BS_ERR_INVALID_ARG;
+    if (N2 % 256 != 0) return FP8BS_ERR_SHAPE;
+    if (!aligned16(sh) || (h != nullptr && !aligned16(h))) return FP8BS_ERR_ALIGN;
+    GemmSpec s = spec_of(FP8BS_OP_FPROP, xq, sx, wq, sw, h, M, N2, K);
+    s.out_q = hq;
+    s.out_s = sh;
+    s.swiglu = true;
     return run_gemm(s, static_cast<cudaStream_t>(stream));
 }
 
@@ -613,6 +631,19 @@ int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* 
     const int64_t want = (groups + 255) / 256;
     const int grid = static_cast<int>(want < 8 * d->sm_count ? want : 8 * d->sm_count);
     e4m3_encode_bits_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(first, n, out);
+    g_launches.fetch_add(1);
+    return launch_status();
+}
+
+int fp8bs_debug_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h, void* stream) {
+    if (!g || !u || !h || n < 0) return FP8BS_ERR_INVALID_ARG;
+    if (n == 0) return FP8BS_OK;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    const int64_t want = (n + 255) / 256;
+    const int grid = static_cast<int>(want < 8 * d->sm_count ? want : 8 * d->sm_count);
+    silu_mul_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(g, u, n, h);
     g_launches.fetch_add(1);
     return launch_status();
 }

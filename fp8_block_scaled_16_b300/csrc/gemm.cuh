@@ -57,6 +57,7 @@
 
 #include <cstdint>
 
+#include "act.cuh"
 #include "ptx.cuh"
 
 namespace fp8bs {
@@ -105,7 +106,7 @@ struct Tile {
     static constexpr int OUT_BOX_BYTES = 32 * 64 * 2;
     static constexpr int OFF_OUT = (OFF_SCALE + SSLOTS * SLOT_FLOATS * 4 + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_OUT + NUM_EPI_WARPS * 2 * OUT_BOX_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 2 * SSLOTS;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 2 * SSLOTS + 8;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -120,6 +121,9 @@ struct Tile {
     static __device__ __forceinline__ uint32_t tempty(int b) { return 2 * STAGES + NBUF + b; }
     static __device__ __forceinline__ uint32_t sfull(int i) { return 2 * STAGES + 2 * NBUF + i; }
     static __device__ __forceinline__ uint32_t sempty(int i) { return 2 * STAGES + 2 * NBUF + SSLOTS + i; }
+    // SwiGLU epilogue: the up half of quadrant q's rows handed to the gate half.
+    static __device__ __forceinline__ uint32_t xfull(int q) { return 2 * STAGES + 2 * NBUF + 2 * SSLOTS + q; }
+    static __device__ __forceinline__ uint32_t xempty(int q) { return 2 * STAGES + 2 * NBUF + 2 * SSLOTS + 4 + q; }
 };
 
 struct Params {
@@ -142,6 +146,13 @@ struct Params {
     // out_s[cols/128][sa_ld] (null: not requested).
     float* out_s;
     int32_t out_q;
+    // Forward product of a gate+up projection whose weight rows alternate
+    // in 128-row blocks (gate block j, then up block j): every output tile's
+    // column halves are the gate and up values of one 128-wide block of
+    // H = SiLU(gate) * up, which the epilogue computes and stores instead of
+    // the tile: BF16 H through tmC (if out_bf16) and its 1x128 quantization
+    // through tmQ / out_s, both [rows][cols/2].
+    int32_t out_swiglu;
     // K splits (1 = none) of the tiles t >= tail_first (0: of every tile).
     // With T = tiles - tail_first split tiles, split s > 0 of tile t is a
     // helper that leaves its FP32 partial in ws slot (s-1)*T + (t-tail_first)
@@ -339,6 +350,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             mbar_init(bar(T::tfull(b)), 1);
             mbar_init(bar(T::tempty(b)), NUM_EPI_WARPS);
         }
+        for (int q = 0; q < 4; q++) {
+            mbar_init(bar(T::xfull(q)), 1);
+            mbar_init(bar(T::xempty(q)), 1);
+        }
         for (int i = 0; i < SSLOTS; i++) {
             mbar_init(bar(T::sfull(i)), 32);   // one cp.async arrival per lane of the scale warp
             mbar_init(bar(T::sempty(i)), NUM_EPI_WARPS);
@@ -503,7 +518,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         const int row = quad * 32 + lane;
         const float* ring = reinterpret_cast<const float*>(smem + T::OFF_SCALE);
         int tb = 0, slot = 0;
-        uint32_t tph = 0, sph = 0;
+        uint32_t tph = 0, sph = 0, xph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
@@ -617,6 +632,112 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                     }
                 }
                 if (!ok) break;
+            }
+            if constexpr (SBMODE == SB_SCALAR) {
+                if (p.out_swiglu) {
+                    // SwiGLU: half 0 holds the gate values of this 128-wide H block,
+                    // half 1 the up values of the same rows and columns.  The up warp
+                    // hands its BF16 row to the gate warp of its quadrant through its
+                    // (otherwise unused) staging buffer: 32 rows x 256 bytes, 16-byte
+                    // chunk c of row r at c ^ (r % 16).
+                    const uint32_t xbuf = sbase + T::OFF_OUT + static_cast<uint32_t>((quad + 4) * 2 * T::OUT_BOX_BYTES);
+                    if (half == 1) {
+                        if (!warp_wait_bounded(bar(T::xempty(quad)), xph ^ 1u, wc)) { ok = false; break; }
+#pragma unroll
+                        for (int c = 0; c < 16; c++) {
+                            const int j = c * 8;
+                            const uint32_t a = xbuf + static_cast<uint32_t>(lane * 256 + ((c ^ (lane & 15)) << 4));
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                         "r"(f32x2_to_bf16x2(acc[j], acc[j + 1])), "r"(f32x2_to_bf16x2(acc[j + 2], acc[j + 3])),
+                                         "r"(f32x2_to_bf16x2(acc[j + 4], acc[j + 5])), "r"(f32x2_to_bf16x2(acc[j + 6], acc[j + 7]))
+                                         : "memory");
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(T::xfull(quad)));
+                        xph ^= 1u;
+                        continue;
+                    }
+                    if (!warp_wait_bounded(bar(T::xfull(quad)), xph, wc)) { ok = false; break; }
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int c = 0; c < 16; c++) {
+                        const int j = c * 8;
+                        uint32_t uw[4];
+                        const uint32_t a = xbuf + static_cast<uint32_t>(lane * 256 + ((c ^ (lane & 15)) << 4));
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(uw[0]), "=r"(uw[1]), "=r"(uw[2]), "=r"(uw[3])
+                                     : "r"(a)
+                                     : "memory");
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const uint32_t gw = f32x2_to_bf16x2(acc[j + 2 * e], acc[j + 2 * e + 1]);
+                            const float h0 = silu_mul_f32(bf16lo_to_f32(gw), bf16lo_to_f32(uw[e]));
+                            const float h1 = silu_mul_f32(bf16hi_to_f32(gw), bf16hi_to_f32(uw[e]));
+                            const uint32_t hw = f32x2_to_bf16x2(h0, h1);
+                            acc[j + 2 * e] = bf16lo_to_f32(hw);
+                            acc[j + 2 * e + 1] = bf16hi_to_f32(hw);
+                            amax = fmaxf(amax, fmaxf(fabsf(acc[j + 2 * e]), fabsf(acc[j + 2 * e + 1])));
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::xempty(quad)));
+                    xph ^= 1u;
+                    // H block nb: BF16 (optional), then its 1x128 quantization.
+                    const bool hvalid = static_cast<int64_t>(mb) * BM + quad * 32 < p.rows;
+                    const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
+                    if (hvalid && p.out_bf16) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int b = 0; b < 2; b++) {
+#pragma unroll
+                            for (int c = 0; c < 8; c++) {
+                                const int j = b * 64 + c * 8;
+                                const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
+                                                                                     ((c ^ (lane & 7)) << 4));
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                             "r"(f32x2_to_bf16x2(acc[j], acc[j + 1])), "r"(f32x2_to_bf16x2(acc[j + 2], acc[j + 3])),
+                                             "r"(f32x2_to_bf16x2(acc[j + 4], acc[j + 5])), "r"(f32x2_to_bf16x2(acc[j + 6], acc[j + 7]))
+                                             : "memory");
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&grp.tmC[g], stage_out, nb * COLS, mb * BM + quad * 32);
+                            tma_store_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, nb * COLS + 64, mb * BM + quad * 32);
+                            bulk_commit_group();
+                        }
+                    }
+                    float sq, inv;
+                    tile_scale(amax, sq, inv);
+                    p.out_s[static_cast<int64_t>(nb) * p.sa_ld + static_cast<int64_t>(mb) * BM + row] = sq;
+                    if (hvalid) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 8; c++) {
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int q = 0; q < 4; q++) {
+                                const int j = c * 16 + q * 4;
+                                wv[q] = e4m3x2(__fmul_rn(acc[j], inv), __fmul_rn(acc[j + 1], inv)) |
+                                        (e4m3x2(__fmul_rn(acc[j + 2], inv), __fmul_rn(acc[j + 3], inv)) << 16);
+                            }
+                            const uint32_t a = stage_out + static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4));
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]),
+                                         "r"(wv[2]), "r"(wv[3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&grp.tmQ[g], stage_out, nb * COLS, mb * BM + quad * 32);
+                            bulk_commit_group();
+                        }
+                    }
+                    continue;
+                }
             }
             // Output boxes that lie wholly past the last row (a token tail) are
             // not stored; TMA clips the rows of a partial box.

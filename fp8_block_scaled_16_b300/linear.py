@@ -126,3 +126,14 @@ def grouped_launch_list(steps, stream=None) -> List[Launch]:
     if wgrad:
         out.append(group("wgrad", wgrad))
     return out
+
+
+def interleave_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor) -> torch.Tensor:
+    """The gate+up weight in the row order fp8bs_gemm_fprop_swiglu_quant
+    reads: 128-row blocks alternating gate block j, up block j ([2I][K] from
+    two [I][K] weights, I a multiple of 128).  A weight layout chosen once,
+    when the weights are loaded."""
+    I, K = w_gate.shape
+    if tuple(w_up.shape) != (I, K) or I % 128:
+        raise ValueError("gate and up weights must both be [I][K] with I a multiple of 128")
+    return torch.stack([w_gate.reshape(I // 128, 128, K), w_up.reshape(I // 128, 128, K)], 1).reshape(2 * I, K)

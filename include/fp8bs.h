@@ -139,6 +139,31 @@ int fp8bs_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq
                            uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * Gate+up forward GEMM with the SwiGLU activation and the down projection's
+ * FP8 input computed in the epilogue:
+ *   H = SiLU(G) * U,  G = X Wg^T, U = X Wu^T  (BF16-rounded, as fprop gives),
+ *   SiLU(g) = g / (1 + e^-g) in FP32, H rounded to BF16, then H's 1x128
+ *   row-wise quantization.
+ *   xq, sx : X as for fp8bs_gemm_fprop ([M][K], [K/128][Mp]).
+ *   wq, sw : the quantized gate+up weight [N2][K] (N2 = 2 I, a multiple of
+ *            256) whose rows alternate in 128-row blocks: rows 256j..256j+127
+ *            are gate rows 128j..128j+127, rows 256j+128..256j+255 the up rows
+ *            of the same outputs (fp8bs_quantize_weight on that interleaved W
+ *            gives wq, sw [N2/128][K/128]).
+ *   h      : BF16 [M][I] output, or NULL to skip it.
+ *   hq, sh : E4M3 [M][I] and FP32 [I/128][Mp] -- what fp8bs_quantize_act
+ *            with FP8BS_ROWWISE writes for H.
+ * e^x is computed by Cody-Waite reduction with a degree-7 Taylor polynomial
+ * (one IEEE operation per step), so every H is a fixed function of G and U;
+ * fp8bs_debug_silu_mul runs the same activation on arrays.
+ * Passage: the activation stays out of the FP8 path (blog section
+ * "FP8：加快 RTX 5090 上的训练"); its output is the down projection's FP8
+ * input, quantized here without a pass over H.
+ */
+int fp8bs_gemm_fprop_swiglu_quant(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, void* h,
+                                  uint8_t* hq, float* sh, int64_t M, int64_t N2, int64_t K, void* stream);
+
+/*
  * Data-gradient GEMM  dX = dY W  (BF16 out [M][K]); contraction over N.
  *   dyq [M][N] E4M3 with sdy [N/128][Mp] (fp8bs_quantize_act on dY, ROWWISE),
  *   wqT [K][N] E4M3 (the transposed payload from fp8bs_quantize_weight),
@@ -306,6 +331,9 @@ int64_t fp8bs_launch_count(void);
  *   fp8bs_debug_e4m3_encode_bits: runs the kernels' FP32->E4M3 encoder on
  *     the FP32 values whose bit patterns are first .. first+n-1, writing n
  *     codes to the device buffer `out`.
+ *   fp8bs_debug_silu_mul: h[i] = bf16(SiLU(g[i]) * u[i]) on BF16 bit patterns
+ *     (device arrays of n elements), the activation of
+ *     fp8bs_gemm_fprop_swiglu_quant.
  *   fp8bs_debug_split_plan: the split-K plan for `tiles` output tiles of
  *     `kblocks` 128-wide contraction blocks on `sms` SMs, host only (no
  *     device needed): out[0] splits (1 = none), out[1] the first split tile
@@ -316,6 +344,7 @@ int fp8bs_debug_set_wait_timeout_ns(int64_t ns);
 int fp8bs_debug_set_fault(int mode);
 int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
 int fp8bs_debug_split_plan(int64_t tiles, int64_t kblocks, int sms, int64_t* out);
+int fp8bs_debug_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h, void* stream);
 
 #ifdef __cplusplus
 }

@@ -83,6 +83,12 @@ def test_validation_before_launch(lib):
     assert fq(fake, fake, fake, fake, None, odd, fake, 128, 256, 128, None) == 3
     assert fq(fake, fake, fake, fake, odd, fake, fake, 128, 256, 128, None) == 3       # optional Y misaligned
     assert fq(fake, fake, fake, fake, None, fake, odd, 128, 256, 128, None) == 3
+    fs = lib.fp8bs_gemm_fprop_swiglu_quant
+    assert fs(fake, fake, fake, fake, None, fake, None, 128, 256, 128, None) == 1      # no scales for Hq
+    assert fs(fake, fake, fake, fake, None, fake, fake, 128, 384, 128, None) == 2      # N2 not a multiple of 256
+    assert fs(fake, fake, fake, fake, odd, fake, fake, 128, 256, 128, None) == 3
+    assert lib.fp8bs_debug_silu_mul(None, fake, 16, fake, None) == 1
+    assert lib.fp8bs_debug_silu_mul(fake, fake, -1, fake, None) == 1
     assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, None, None) == 1
     assert lib.fp8bs_debug_e4m3_encode_bits(0xFFFFFFF0, 32, fake, None) == 2
     assert lib.fp8bs_debug_e4m3_encode_bits(0, 16, odd, None) == 3

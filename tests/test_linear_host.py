@@ -5,7 +5,9 @@ CPU here; no call is run."""
 import pytest
 
 from fp8_block_scaled_16_b300 import binding as B
-from fp8_block_scaled_16_b300.linear import Fp8LinearStep, grouped_launch_list
+import torch
+
+from fp8_block_scaled_16_b300.linear import Fp8LinearStep, grouped_launch_list, interleave_gate_up
 
 
 def act_bytes(rows, cols, layouts):
@@ -56,3 +58,16 @@ def test_grouped_step_rejects_more_linears_than_a_group_holds():
     steps = [(Fp8LinearStep(128, 256, 128, device="cpu"), None, None, None)] * (B.GROUP_MAX + 1)
     with pytest.raises(ValueError):
         grouped_launch_list(steps)
+
+
+def test_interleave_gate_up_row_order():
+    I, K = 384, 8
+    wg = torch.arange(I * K, dtype=torch.float32).reshape(I, K)
+    wu = -wg - 1
+    w = interleave_gate_up(wg, wu)
+    assert tuple(w.shape) == (2 * I, K)
+    for j in range(I // 128):
+        assert torch.equal(w[256 * j:256 * j + 128], wg[128 * j:128 * j + 128])
+        assert torch.equal(w[256 * j + 128:256 * j + 256], wu[128 * j:128 * j + 128])
+    with pytest.raises(ValueError):
+        interleave_gate_up(wg[:100], wu[:100])
