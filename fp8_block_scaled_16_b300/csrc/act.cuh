@@ -45,6 +45,11 @@ __device__ __forceinline__ float silu_mul_f32(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, d), u);
 }
 
+// The same as a called function: the GEMM epilogue evaluates it for 128
+// values per thread, and 128 inlined copies would crowd the instruction
+// cache that the K-block loop runs from.
+__device__ __noinline__ float silu_mul_call(float g, float u) { return silu_mul_f32(g, u); }
+
 // Test kernel: h[i] = bf16(SiLU(g[i]) * u[i]) on BF16 bit patterns.
 __global__ void silu_mul_kernel(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;

@@ -41,7 +41,7 @@ struct DeviceInfo {
     bool arch_ok = false;
     int sm_count = 0;
     uint32_t* status = nullptr;
-    bool gemm_attr_set[2][2] = {{false, false}, {false, false}};  // [scale mode][grouped]
+    bool gemm_attr_set[2][2][3] = {};  // [scale mode][grouped][epilogue variant]
     // Caller-registered scratch for split-K GEMMs (fp8bs_set_workspace).
     uint8_t* ws = nullptr;
     int64_t ws_bytes = 0;
@@ -271,15 +271,15 @@ int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap*
     return FP8BS_OK;
 }
 
-template <int SBMODE, int G>
+template <int SBMODE, int G, int EPI = gemm::EPI_PLAIN>
 int launch_group(DeviceInfo* d, const gemm::Group<G>& grp, cudaStream_t st) {
     using namespace gemm;
     using T = Tile<256>;
     const int64_t units = grp.first_unit[grp.count];
     if (units <= 0) return FP8BS_OK;
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
-    auto kern = gemm_kernel<SBMODE, 256, G>;
-    bool& attr = d->gemm_attr_set[SBMODE][G > 1 ? 1 : 0];
+    auto kern = gemm_kernel<SBMODE, 256, G, EPI>;
+    bool& attr = d->gemm_attr_set[SBMODE][G > 1 ? 1 : 0][EPI];
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
             return launch_status();
@@ -317,7 +317,10 @@ int run_gemm(const GemmSpec& s, cudaStream_t st) {
     grp.count = 1;
     grp.first_unit[0] = 0;
     grp.first_unit[1] = static_cast<int32_t>(units);
-    return s.sbmode == SB_VECTOR ? launch_group<SB_VECTOR, 1>(d, grp, st) : launch_group<SB_SCALAR, 1>(d, grp, st);
+    if (s.sbmode == SB_VECTOR) return launch_group<SB_VECTOR, 1>(d, grp, st);
+    if (s.swiglu) return launch_group<SB_SCALAR, 1, EPI_SWIGLU>(d, grp, st);
+    if (s.out_q != nullptr) return launch_group<SB_SCALAR, 1, EPI_FP8>(d, grp, st);
+    return launch_group<SB_SCALAR, 1>(d, grp, st);
 }
 
 }  // namespace

@@ -78,6 +78,10 @@ static_assert(THREADS == 384, "warp roles");
 static_assert(128 * REGS_CTRL + NUM_EPI_WARPS * 32 * REGS_EPI <= THREADS * 168, "register split");
 
 enum : int { SB_SCALAR = 0, SB_VECTOR = 1 };
+// Epilogue variants of the forward product, each its own kernel so that the
+// plain kernel carries none of the others' code: the tile as BF16 (or FP32
+// reduce-adds); plus its 1x128 FP8 quantization; the SwiGLU block instead.
+enum : int { EPI_PLAIN = 0, EPI_FP8 = 1, EPI_SWIGLU = 2 };
 
 // Shared-memory plan for a 128 x BN tile.
 template <int BN>
@@ -328,8 +332,9 @@ __device__ __forceinline__ void promote_rank1(float (&acc)[N], int base_lo, int 
     }
 }
 
-template <int SBMODE, int BN, int G>
+template <int SBMODE, int BN, int G, int EPI>
 __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ Group<G> grp) {
+    static_assert(EPI == EPI_PLAIN || (SBMODE == SB_SCALAR && G == 1), "FP8 epilogues: single forward products");
     using T = Tile<BN>;
     constexpr int STAGES = T::STAGES, NBUF = T::NBUF, COLS = T::COLS;
     extern __shared__ uint8_t smem_raw[];
@@ -634,7 +639,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                 if (!ok) break;
             }
             if constexpr (SBMODE == SB_SCALAR) {
-                if (p.out_swiglu) {
+                if constexpr (EPI == EPI_SWIGLU) {
                     // SwiGLU: half 0 holds the gate values of this 128-wide H block,
                     // half 1 the up values of the same rows and columns.  The up warp
                     // hands its BF16 row to the gate warp of its quadrant through its
@@ -671,8 +676,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
 #pragma unroll
                         for (int e = 0; e < 4; e++) {
                             const uint32_t gw = f32x2_to_bf16x2(acc[j + 2 * e], acc[j + 2 * e + 1]);
-                            const float h0 = silu_mul_f32(bf16lo_to_f32(gw), bf16lo_to_f32(uw[e]));
-                            const float h1 = silu_mul_f32(bf16hi_to_f32(gw), bf16hi_to_f32(uw[e]));
+                            const float h0 = silu_mul_call(bf16lo_to_f32(gw), bf16lo_to_f32(uw[e]));
+                            const float h1 = silu_mul_call(bf16hi_to_f32(gw), bf16hi_to_f32(uw[e]));
                             const uint32_t hw = f32x2_to_bf16x2(h0, h1);
                             acc[j + 2 * e] = bf16lo_to_f32(hw);
                             acc[j + 2 * e + 1] = bf16hi_to_f32(hw);
@@ -852,7 +857,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                 }
             }
             if constexpr (SBMODE == SB_SCALAR) {
-                if (p.out_q && jvalid) {
+                if (EPI == EPI_FP8 && jvalid) {  // compile-time false outside the FP8 kernel
                     // FP8 output for the next linear: this thread holds one row's 128
                     // columns, i.e. one whole 1x128 tile.  Round to BF16 (the value the
                     // BF16 output holds), amax, the scheme's scale, E4M3 cast -- the
