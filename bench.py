@@ -284,47 +284,73 @@ def sweep(peaks, fp8_peak):
 def e2e_run(wl, steps_data, steps):
     """The step through the public API with host buffers: every step copies
     each linear's X, W, dY in from pinned host memory and its Y, dX, dW back
-    out, and the host waits for the step's results.  Three streams pipeline
-    the linears: linear i+1's inputs are copied in while linear i computes and
-    linear i-1's outputs are copied out (PCIe carries both directions at
-    once); events order each linear's copy-in -> library calls -> copy-out."""
-    host_in, host_out, dev, h2d, d2h = [], [], [], 0, 0
+    out, and the host waits for each step's results.  Three streams pipeline
+    the work: a linear's inputs are copied in while the previous linear
+    computes and the one before is copied out (PCIe carries both directions
+    at once), and the next step's first copies start while this step's last
+    outputs are still coming back (the host output buffers alternate between
+    steps, so a step's results stay intact until the host has read them).
+    Events order every buffer's reuse: a linear's device inputs are
+    overwritten only after its previous computation, its device outputs only
+    after their previous copy-out."""
+    host_in, host_out, dev, h2d, d2h = [], [[], []], [], 0, 0
+    outs_dev = []
     for st, d in steps_data:
         hi = {k: v.cpu().pin_memory() for k, v in d.items()}
         host_in.append(hi)
         h2d += sum(v.numel() * v.element_size() for v in hi.values())
         outs = [t for t in (st.y, st.dx, st.dw) if t is not None]
-        ho = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        host_out.append((outs, ho))
+        outs_dev.append(outs)
+        for par in (0, 1):
+            host_out[par].append([torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs])
         d2h += sum(t.numel() * t.element_size() for t in outs)
         dev.append({k: torch.empty_like(v) for k, v in d.items()})
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     lls = [st.launch_list(dv["x"], dv["w"], dv.get("dy"), stream=s_run) for (st, _), dv in zip(steps_data, dev)]
+    n = len(steps_data)
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_run = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    started = [False] * n
 
-    def one():
-        for hi, dv, ll, (outs, ho) in zip(host_in, dev, lls, host_out):
+    def issue(k):
+        par = k & 1
+        for i in range(n):
             with torch.cuda.stream(s_in):
-                for k in hi:
-                    dv[k].copy_(hi[k], non_blocking=True)
-                copied = torch.cuda.Event()
-                copied.record(s_in)
-            s_run.wait_event(copied)
+                if started[i]:
+                    s_in.wait_event(ev_run[i])        # the previous computation has read the inputs
+                for key, h in host_in[i].items():
+                    dev[i][key].copy_(h, non_blocking=True)
+                ev_in[i].record(s_in)
+            s_run.wait_event(ev_in[i])
+            if started[i]:
+                s_run.wait_event(ev_out[i])           # the previous copy-out has read the outputs
             with torch.cuda.stream(s_run):
-                for l in ll:
+                for l in lls[i]:
                     l.run()
-                done = torch.cuda.Event()
-                done.record(s_run)
-            s_out.wait_event(done)
+                ev_run[i].record(s_run)
+            s_out.wait_event(ev_run[i])
             with torch.cuda.stream(s_out):
-                for t, h in zip(outs, ho):
+                for t, h in zip(outs_dev[i], host_out[par][i]):
                     h.copy_(t, non_blocking=True)
-        s_out.synchronize()  # the host reads the step's results
-        s_run.synchronize()
+                ev_out[i].record(s_out)
+            started[i] = True
+        done = torch.cuda.Event()
+        done.record(s_out)
+        return done
 
-    one()
+    def read(done, k):
+        done.synchronize()                            # the host reads step k's results
+        return float(host_out[k & 1][-1][-1].view(-1)[0])
+
+    read(issue(0), 0)
     t = time.perf_counter()
-    for _ in range(steps):
-        one()
+    prev = issue(1)
+    for k in range(2, steps + 1):
+        cur = issue(k)
+        read(prev, k - 1)
+        prev = cur
+    read(prev, steps)
     dt = (time.perf_counter() - t) / steps
     return dt, h2d, d2h
 
@@ -558,7 +584,8 @@ def run_ours(args):
                          "ms_per_step": round(dt_max * 1e3, 2), "steps": e2e_steps,
                          "note": "every step copies X, W, dY in from pinned host memory and Y, dX, dW back out "
                                  "around the same library calls; copy-in, compute and copy-out streams pipeline the "
-                                 "four linears; host clock, the host waits for each step's results"}
+                                 "four linears and the next step's first copies overlap this step's last; host "
+                                 "clock, the host waits for and reads each step's results"}
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu:
         fl, sec = cpu_sample(list(zip(wl.linears, data)), args.cpu_feats, args.cpu_rows)
         result["cpu_baseline"] = {
