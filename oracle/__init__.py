@@ -23,6 +23,8 @@ Pinned by ``tests/test_oracle_*.py`` (CPU only):
   * SwiGLU activation (tests/test_oracle_activation.py): its exponential
     within 1 ulp of float64 e^x, SiLU(g)*u within one BF16 ulp of the
     float64 formula on every BF16 g in [-24, 24], and its special cases.
+tests/test_oracle_mutants.py plants one plausible mistake at a time in a
+copy of the C source and checks that some pin fails.
 """
 from __future__ import annotations
 
@@ -37,13 +39,20 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8bs_oracle.c")
 _LIB = os.path.join(_HERE, "liborc_fp8bs.so")
 _CFLAGS = ["-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11"]
+SOURCE, CFLAGS = _SRC, _CFLAGS  # for tests that compile altered copies
 
 _lib = None
 _lock = threading.Lock()
 
 
 def build(force: bool = False) -> str:
-    """Compile the C oracle (gcc) next to its source; returns the .so path."""
+    """Compile the C oracle (gcc) next to its source; returns the .so path.
+    Test hook: FP8BS_ORACLE_LIB names a library built elsewhere from a
+    deliberately altered copy of the source (tests/test_oracle_mutants.py),
+    which the pins must then reject."""
+    alt = os.environ.get("FP8BS_ORACLE_LIB")
+    if alt:
+        return alt
     if (not force and os.path.exists(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
