@@ -132,3 +132,39 @@ def test_debug_setters(lib):
     assert lib.fp8bs_debug_set_wait_timeout_ns(-1) == 1
     assert lib.fp8bs_debug_set_wait_timeout_ns(0) == 0
     assert lib.fp8bs_launch_count() >= 0
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "fp8bs.h"
+
+int main(void) {
+    /* argument checks answer before any device work, so this runs without a GPU */
+    int64_t plan[4];
+    fp8bs_gemm_args g;
+    memset(&g, 0, sizeof g);
+    g.op = FP8BS_OP_FPROP;
+    if (fp8bs_gemm_fprop(NULL, NULL, NULL, NULL, NULL, 128, 256, 128, NULL) != FP8BS_ERR_INVALID_ARG) return 1;
+    if (fp8bs_quantize_act((const void*)0x10000, 128, 100, FP8BS_ROWWISE, (uint8_t*)0x10000, (float*)0x10000,
+                           NULL, NULL, NULL) != FP8BS_ERR_SHAPE) return 2;
+    if (fp8bs_gemm_group(&g, 0, NULL) != FP8BS_ERR_INVALID_ARG) return 3;
+    if (fp8bs_debug_split_plan(768, 64, 148, plan) != FP8BS_OK || plan[0] != 5 || plan[1] != 740) return 4;
+    if (strcmp(fp8bs_status_string(FP8BS_OK), "FP8BS_OK") != 0) return 5;
+    printf("ok\n");
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_the_library_links(tmp_path, lib):
+    """A C program (gcc, C11, no C++) includes the header, links the library
+    and gets the documented answers from calls that fail validation."""
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(build_mod.LIB)
+    subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-L", libdir, "-lfp8bs", f"-Wl,-rpath,{libdir}", "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
