@@ -17,11 +17,13 @@
 //       into a 3-stage shared-memory ring (128-byte swizzle);
 //   warp 1: MMA issuer -- four tcgen05.mma (K = 32 each) per K block into one
 //       of two 128 x 256 FP32 TMEM buffers (all 512 columns), the first with
-//       accumulate off, then commits to free the smem stage and to publish
-//       the buffer;
-//   warp 2: scale loader -- per K block the 128 row scales (and, for the
-//       weight gradient, the 256 column scales, regrouped for the epilogue's
-//       layout) into an 8-slot shared-memory ring with cp.async;
+//       accumulate off, then one commit whose barrier both frees the smem
+//       stage and tells the promotion warps that the buffer is complete;
+//   warp 2: scale loader -- into an 8-slot shared-memory ring with cp.async:
+//       forward / data gradient, per slot the 128 row scales and the two
+//       weight scales of 4 consecutive K blocks; weight gradient, per slot
+//       one K block's 128 row scales and 256 column scales (regrouped for
+//       the epilogue's layout);
 //   warp 3: idle (it completes the first warpgroup, whose registers are
 //       handed to the epilogue warpgroups with setmaxnreg);
 //   warps 4..11: promotion + epilogue -- each warp owns a 32-lane TMEM
@@ -100,7 +102,14 @@ struct Tile {
     static constexpr int SB_GROUP = 36;
     static constexpr int SB_HALF = 4 * SB_GROUP;
     static constexpr int SB_FLOATS = 2 * SB_HALF;
-    static constexpr int SLOT_FLOATS = SA_FLOATS + SB_FLOATS;
+    // Forward / data gradient: one slot carries the scales of SBATCH K
+    // blocks -- row scales [SBATCH][128], then the weight scales of the
+    // tile's two 128-column halves [SBATCH][2] -- so the promotion warps
+    // synchronise on the ring once per SBATCH blocks.
+    static constexpr int SBATCH = 4;
+    static constexpr int SCALAR_SLOT_FLOATS = SBATCH * (SA_FLOATS + 2);
+    static constexpr int SLOT_FLOATS =
+        (SA_FLOATS + SB_FLOATS) > SCALAR_SLOT_FLOATS ? (SA_FLOATS + SB_FLOATS) : SCALAR_SLOT_FLOATS;
     static constexpr int COLS = BN / 2;                           // columns per epilogue warp
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -110,24 +119,26 @@ struct Tile {
     static constexpr int OUT_BOX_BYTES = 32 * 64 * 2;
     static constexpr int OFF_OUT = (OFF_SCALE + SSLOTS * SLOT_FLOATS * 4 + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_OUT + NUM_EPI_WARPS * 2 * OUT_BOX_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 2 * SSLOTS + 8;
+    static constexpr int NUM_BARS = 2 * STAGES + NBUF + 2 * SSLOTS + 8;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment for 128-byte swizzle");
     static_assert(COLS == 128, "epilogue chunking assumes 128 columns per warp");
-    static_assert(SB_FLOATS >= BN && (SA_FLOATS + SB_FLOATS) % 4 == 0, "scale slot layout");
+    static_assert(SB_FLOATS >= BN && (SA_FLOATS + SB_FLOATS) % 4 == 0 && SLOT_FLOATS % 4 == 0, "scale slot layout");
     static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
     // barrier indices
     static __device__ __forceinline__ uint32_t full(int s) { return s; }
     static __device__ __forceinline__ uint32_t empty(int s) { return STAGES + s; }
-    static __device__ __forceinline__ uint32_t tfull(int b) { return 2 * STAGES + b; }
-    static __device__ __forceinline__ uint32_t tempty(int b) { return 2 * STAGES + NBUF + b; }
-    static __device__ __forceinline__ uint32_t sfull(int i) { return 2 * STAGES + 2 * NBUF + i; }
-    static __device__ __forceinline__ uint32_t sempty(int i) { return 2 * STAGES + 2 * NBUF + SSLOTS + i; }
+    // empty(s) completes when the MMAs that read stage s have finished: it
+    // frees the stage for the producer and also tells the promotion warps
+    // that the accumulator buffer those MMAs wrote is complete.
+    static __device__ __forceinline__ uint32_t tempty(int b) { return 2 * STAGES + b; }
+    static __device__ __forceinline__ uint32_t sfull(int i) { return 2 * STAGES + NBUF + i; }
+    static __device__ __forceinline__ uint32_t sempty(int i) { return 2 * STAGES + NBUF + SSLOTS + i; }
     // SwiGLU epilogue: the up half of quadrant q's rows handed to the gate half.
-    static __device__ __forceinline__ uint32_t xfull(int q) { return 2 * STAGES + 2 * NBUF + 2 * SSLOTS + q; }
-    static __device__ __forceinline__ uint32_t xempty(int q) { return 2 * STAGES + 2 * NBUF + 2 * SSLOTS + 4 + q; }
+    static __device__ __forceinline__ uint32_t xfull(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + q; }
+    static __device__ __forceinline__ uint32_t xempty(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + 4 + q; }
 };
 
 struct Params {
@@ -247,6 +258,16 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, 
     }
 }
 
+// Bounded wait for the warps on the hand-off path, without a warp vote:
+// the warp runs converged, and every lane executes the same try_wait on the
+// same barrier word (and on the slow path reads the same timer and abort
+// flag), so the result is the same in every lane.  The vote of
+// warp_wait_bounded costs measurable time on a path the tensor pipe waits on.
+__device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded(bar, parity, w);
+}
+
 // Bounded wait used while tearing down after an abort: ignores the abort
 // flag, only the time limit ends it.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
@@ -351,10 +372,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             mbar_init(bar(T::full(s)), 1);
             mbar_init(bar(T::empty(s)), 1);
         }
-        for (int b = 0; b < NBUF; b++) {
-            mbar_init(bar(T::tfull(b)), 1);
-            mbar_init(bar(T::tempty(b)), NUM_EPI_WARPS);
-        }
+        for (int b = 0; b < NBUF; b++) mbar_init(bar(T::tempty(b)), NUM_EPI_WARPS);
         for (int q = 0; q < 4; q++) {
             mbar_init(bar(T::xfull(q)), 1);
             mbar_init(bar(T::xempty(q)), 1);
@@ -440,14 +458,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         int stage = 0, tb = 0;
         uint32_t ph = 0, tph = 0;
         bool ok = true, issued = false;
-        int last_tb = 0;
-        uint32_t last_tph = 0;
+        int last_stage = 0;
+        uint32_t last_ph = 0;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
             (void)num_tiles;
             for (int kb = w.kb0; kb < w.kb1; kb++) {
-                if (!warp_wait_bounded(bar(T::tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
-                if (!warp_wait_bounded(bar(T::full(stage)), ph, wc)) { ok = false; break; }
+                // The operands are usually in place long before the buffer is free.
+                if (!uniform_wait(bar(T::full(stage)), ph, wc)) { ok = false; break; }
+                if (!uniform_wait(bar(T::tempty(tb)), tph ^ 1u, wc)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t a0 = sbase + T::OFF_A + stage * T::A_BYTES;
@@ -457,18 +476,19 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                     for (int kk = 0; kk < BK / 32; kk++)
                         mma_f8(d, sdesc_k_major_sw128(a0 + kk * 32), sdesc_k_major_sw128(b0 + kk * 32), idesc,
                                kk > 0 ? 1u : 0u);
+                    // One commit per K block: its barrier frees the stage and
+                    // tells the promotion warps that the buffer is complete.
                     mma_commit(bar(T::empty(stage)));
-                    mma_commit(bar(T::tfull(tb)));
                 }
                 __syncwarp();
                 issued = true;
-                last_tb = tb;
-                last_tph = tph;
+                last_stage = stage;
+                last_ph = ph;
                 if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 if (++tb == NBUF) { tb = 0; tph ^= 1u; }
             }
         }
-        if (!ok && issued && lane == 0) drain_wait(bar(T::tfull(last_tb)), last_tph, p0.timeout_ns);
+        if (!ok && issued && lane == 0) drain_wait(bar(T::empty(last_stage)), last_ph, p0.timeout_ns);
         __syncwarp();
       } else if (warp == 2) {
         // ------------------------------------------------ scale loader
@@ -479,12 +499,28 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
             const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
-            for (int kb = w.kb0; kb < w.kb1; kb++) {
+            // One slot per K block (weight gradient) or per SBATCH K blocks.
+            constexpr int step = SBMODE == SB_SCALAR ? T::SBATCH : 1;
+            for (int kb = w.kb0; kb < w.kb1; kb += step) {
                 if (!warp_wait_bounded(bar(T::sempty(slot)), sph ^ 1u, wc)) { ok = false; break; }
                 const uint32_t dst = ring + static_cast<uint32_t>(slot * T::SLOT_FLOATS * 4);
                 const float* sa_src = p.sa + static_cast<int64_t>(kb) * p.sa_ld + mb * BM;
                 if constexpr (SBMODE == SB_SCALAR) {
-                    cp_async_16(dst + lane * 16, sa_src + lane * 4);
+                    // Row scales of blocks kb .. kb+n-1 at [j][128]; the weight scale
+                    // of column half h of block kb+j at SBATCH*128 + 2j + h (a half past
+                    // the output's last column block copies any valid scale: its
+                    // results are never stored).
+                    const int n = w.kb1 - kb < T::SBATCH ? w.kb1 - kb : T::SBATCH;
+                    for (int j = 0; j < n; j++)
+                        cp_async_16(dst + static_cast<uint32_t>(j * T::SA_FLOATS * 4 + lane * 16),
+                                    sa_src + static_cast<int64_t>(j) * p.sa_ld + lane * 4);
+                    if (lane < 2 * n) {
+                        const int j = lane >> 1, h = lane & 1;
+                        int jbh = (nb * BN + h * 128) >> 7;
+                        if (jbh >= p.nb_valid) jbh = 0;
+                        cp_async_4(dst + static_cast<uint32_t>((T::SBATCH * T::SA_FLOATS + 2 * j + h) * 4),
+                                   p.sb + jbh * p.sb_stride_j + (kb + j) * p.sb_stride_b);
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
@@ -522,8 +558,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         const int half = ew >> 2;    // column half of the tile
         const int row = quad * 32 + lane;
         const float* ring = reinterpret_cast<const float*>(smem + T::OFF_SCALE);
-        int tb = 0, slot = 0;
-        uint32_t tph = 0, sph = 0, xph = 0;
+        int tb = 0, slot = 0, stage = 0;
+        uint32_t sph = 0, xph = 0, ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
@@ -534,25 +570,38 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             float acc[COLS];
 #pragma unroll
             for (int i = 0; i < COLS; i++) acc[i] = 0.0f;
-            float sb_next = 0.0f;
-            if (SBMODE == SB_SCALAR && jvalid) sb_next = __ldg(p.sb + jb * p.sb_stride_j + w.kb0 * p.sb_stride_b);
+            (void)jvalid;
+            // Scale products sa * sb of the next K blocks of a batch (forward /
+            // data gradient), shifted down one per block.
+            float sc1 = 0.0f, sc2 = 0.0f, sc3 = 0.0f;
+            static_assert(T::SBATCH == 4, "the batch is unpacked into sc1..sc3");
             for (int kb = w.kb0; kb < w.kb1; kb++) {
-                const float sb_cur = sb_next;
-                if (SBMODE == SB_SCALAR && jvalid && kb + 1 < w.kb1)
-                    sb_next = __ldg(p.sb + jb * p.sb_stride_j + (kb + 1) * p.sb_stride_b);
-                if (!warp_wait_bounded(bar(T::sfull(slot)), sph, wc)) { ok = false; break; }
-                const float* sl = ring + slot * T::SLOT_FLOATS;
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
                                        static_cast<uint32_t>(tb * BN + half * COLS);
                 uint32_t ra[32], rb[32];
                 if constexpr (SBMODE == SB_SCALAR) {
                     // Accumulator slice in the .32x32b layout: thread = row, register =
                     // column; one scale per thread per K block.
-                    const float sc = __fmul_rn(sl[row], sb_cur);
-                    // Only the row scale is needed from the slot: free it now.
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(T::sempty(slot)));
-                    if (!warp_wait_bounded(bar(T::tfull(tb)), tph, wc)) { ok = false; break; }
+                    float sc;
+                    if (((kb - w.kb0) & (T::SBATCH - 1)) == 0) {
+                        if (!uniform_wait(bar(T::sfull(slot)), sph, wc)) { ok = false; break; }
+                        const float* sl = ring + slot * T::SLOT_FLOATS;
+                        const float* sw2 = sl + T::SBATCH * T::SA_FLOATS + half;
+                        const int n = w.kb1 - kb;
+                        sc = __fmul_rn(sl[row], sw2[0]);
+                        if (n > 1) sc1 = __fmul_rn(sl[T::SA_FLOATS + row], sw2[2]);
+                        if (n > 2) sc2 = __fmul_rn(sl[2 * T::SA_FLOATS + row], sw2[4]);
+                        if (n > 3) sc3 = __fmul_rn(sl[3 * T::SA_FLOATS + row], sw2[6]);
+                        // The batch's scales are in registers: free the slot now.
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(T::sempty(slot)));
+                        if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
+                    } else {
+                        sc = sc1;
+                        sc1 = sc2;
+                        sc2 = sc3;
+                    }
+                    if (!uniform_wait(bar(T::empty(stage)), ph, wc)) { ok = false; break; }
                     tc_fence_after();
                     // Two 32-column chunks in flight per wait; the TMEM buffer is
                     // released as soon as the last chunk is in registers.
@@ -577,9 +626,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                     // needs 8 shared-memory loads of column scales per K block instead of
                     // 32 with one row per thread.  acc[32L + i]: L = 0,1 lanes 0-15 and
                     // L = 2,3 lanes 16-31 of the quadrant; L even columns 0-63, odd 64-127.
+                    if (!warp_wait_bounded(bar(T::sfull(slot)), sph, wc)) { ok = false; break; }
+                    const float* sl = ring + slot * T::SLOT_FLOATS;
                     const float4 sa4 = *reinterpret_cast<const float4*>(sl + quad * 32 + 4 * (lane >> 2));
                     const float* cs = sl + T::SA_FLOATS + half * T::SB_HALF + (lane & 3) * T::SB_GROUP;
-                    if (!warp_wait_bounded(bar(T::tfull(tb)), tph, wc)) { ok = false; break; }
+                    if (!uniform_wait(bar(T::empty(stage)), ph, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t thi = taddr + (16u << 16);
                     tmem_ld_16x256b_x8(taddr, ra);
@@ -597,9 +648,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                     promote_rank1(acc, 32, 96, ra, rb, sa4, cs + 16);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(T::sempty(slot)));
+                    if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
                 }
-                if (++tb == NBUF) { tb = 0; tph ^= 1u; }
-                if (++slot == SSLOTS) { slot = 0; sph ^= 1u; }
+                if (++tb == NBUF) tb = 0;
+                if (++stage == STAGES) { stage = 0; ph ^= 1u; }
             }
             if (!ok) break;
             if (w.split) {
