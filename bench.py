@@ -394,6 +394,74 @@ def cpu_sample(lin_data, feats, rows, tokens=128):
     return flops, time.perf_counter() - t
 
 
+def cpu_per_config(rows_timed=32, rows_checked=256):
+    """The oracle per configuration, single-threaded, inputs drawn by the CPU
+    recipe (the parity tests' inputs):
+      - quantizers on whole tensors: X both ways (1x128 and 128x1
+        transposed) and W (128x128 with W^T), as GB/s of algorithmic bytes;
+      - each GEMM on the first `rows_timed` of the `rows_checked` seeded
+        output rows the parity tests check (weight gradient: the first
+        `rows_timed` output features), then the time of all checked rows
+        and of the full GEMM extrapolated from the per-row time (labelled).
+    The tiny configuration's forward product is timed on its full output."""
+    import numpy as np
+
+    import oracle
+
+    def timed(f):
+        t = time.perf_counter()
+        r = f()
+        return r, time.perf_counter() - t
+
+    res = {}
+    t_all = time.perf_counter()
+    for name, wl in inputs.WORKLOADS.items():
+        data = inputs.make_linear_inputs(wl, device="cpu")
+        per_lin = {}
+        for lin, d in zip(wl.linears, data):
+            M, K, N = lin.tokens, lin.in_features, lin.out_features
+            x, w = d["x"], d["w"]
+            out = {}
+            (xq, sx), t = timed(lambda: oracle.quant_rowwise_1x128(x))
+            out["quant_x_rowwise"] = {"s": round(t, 3), "GB/s": round(M * K * (3 + 4 / 128) / t / 1e9, 3)}
+            wq, _, sw = None, None, None
+            (wq, _, sw), t = timed(lambda: oracle.quant_weight_128x128(w, want_t=True))
+            out["quant_w"] = {"s": round(t, 3), "GB/s": round(N * K * 4.0 / t / 1e9, 3)}
+            full = M <= rows_timed * 8 and name.startswith("tiny")
+            rows = (np.arange(M) if full else
+                    inputs.sample_rows(M, wl.seed + 1000, rows_checked).numpy()[:rows_timed])
+
+            def gemm_entry(op, fn, n_rows_total, cols, kc, nrows):
+                (_, sec) = timed(fn)
+                per_row = sec / nrows
+                e = {"rows_timed": int(nrows), "s_timed": round(sec, 3),
+                     "GFLOP/s": round(2 * nrows * cols * kc / sec / 1e9, 3)}
+                if nrows < n_rows_total:
+                    e["s_256_rows_extrapolated"] = round(per_row * min(rows_checked, n_rows_total), 3)
+                    e["s_full_extrapolated"] = round(per_row * n_rows_total, 2)
+                out[op] = e
+
+            gemm_entry("fprop", lambda: oracle.gemm_fprop(xq, sx, wq, sw, rows=rows), M, N, K, rows.size)
+            if "dgrad" in lin.ops:
+                dyq, sdy = oracle.quant_rowwise_1x128(d["dy"][torch.as_tensor(rows)])
+                gemm_entry("dgrad", lambda: oracle.gemm_dgrad(dyq, sdy, wq, sw), M, K, N, rows.size)
+            if "wgrad" in lin.ops:
+                (xTq, sxT), t = timed(lambda: oracle.quant_colwise_128x1_T(x))
+                out["quant_x_colwise_T"] = {"s": round(t, 3), "GB/s": round(M * K * (3 + 4 / 128) / t / 1e9, 3)}
+                dyTq, sdyT = oracle.quant_colwise_128x1_T(d["dy"][:, :128].contiguous())
+                nr = min(rows_timed, 128)
+                gemm_entry("wgrad", lambda: oracle.gemm_wgrad(dyTq, sdyT, xTq, sxT, rows=np.arange(nr)),
+                           N, K, padded(M), nr)
+            per_lin[lin.name] = out
+        res[name] = per_lin if len(per_lin) > 1 else next(iter(per_lin.values()))
+        del data
+    return res, time.perf_counter() - t_all
+
+
+def padded(m):
+    return (m + 127) // 128 * 128
+
+
 def sample_note(feats, rows, tokens=128):
     return (f"each linear restricted to its first {tokens} tokens and first {feats} output features (all input "
             f"features): X and dY quantized both ways, W[:{feats}] quantized 128x128, {rows} output rows of "
@@ -571,6 +639,8 @@ def run_ours(args):
                          f"L2 126 MB)",
                    "inputs": "drawn on the GPU with torch's CUDA generator (distributions as in inputs.py)",
                    "parallelism": f"independent replicas x{ranks.world}" if ranks.world > 1 else "single GPU"},
+        "regime": ("sustained" if long_region else "burst") + f" (timed region {total_ms / 1e3:.2f} s; "
+                  "burst < 2 s, compared with the burst peak)",
         "roofline": roof, "breakdown": breakdown, "gpu_launches": launched,
         "gpu_launches_expected": launches_step * args.steps, "clocks": clk,
     }
@@ -589,8 +659,17 @@ def run_ours(args):
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu:
         fl, sec = cpu_sample(list(zip(wl.linears, data)), args.cpu_feats, args.cpu_rows)
         result["cpu_baseline"] = {
-            "value": fl / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "value": fl / sec / 1e12, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": sample_note(args.cpu_feats, args.cpu_rows) + f", {sec:.1f} s"}
+        if not args.no_cpu_configs:
+            per_cfg, sec_cfg = cpu_per_config()
+            result["cpu_baseline"]["per_config"] = per_cfg
+            result["cpu_baseline"]["per_config_note"] = (
+                f"every configuration, single-threaded oracle, CPU-recipe inputs ({sec_cfg:.0f} s in all): quantizers "
+                "on whole tensors (GB/s of algorithmic bytes); GEMMs timed on the first 32 of the 256 seeded rows the "
+                "parity tests check (weight gradient: the first 32 output features), with the time of all 256 rows "
+                "and of the full GEMM extrapolated from the per-row time; the tiny configuration's forward product in "
+                "full")
     if not args.no_grouped:
         from fp8_block_scaled_16_b300.linear import grouped_launch_list
 
@@ -657,6 +736,23 @@ def run_reference(args):
     }), flush=True)
 
 
+def free_port():
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n):
+    """`--gpus N` without a rank environment: start N ranks of this same
+    command line under torch.distributed.run (one process per GPU, rendezvous
+    on 127.0.0.1) and return their exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -673,9 +769,21 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-grouped", action="store_true", help="skip the grouped-launch step")
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-cpu-configs", action="store_true", help="skip the per-configuration oracle timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        if args.impl == "ours" and torch.cuda.device_count() < args.gpus:
+            sys.exit(f"bench.py: --gpus {args.gpus} needs {args.gpus} visible CUDA devices, "
+                     f"found {torch.cuda.device_count()}")
+        sys.exit(launch_ranks(args.gpus))
+    if world is not None and int(world) != args.gpus:
+        ap.error(f"--gpus {args.gpus} does not match WORLD_SIZE={world}")
+    print(f"[bench] rank {os.environ.get('RANK', '0')}/{world or 1} ({args.impl} arm)", file=sys.stderr, flush=True)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -22,6 +22,8 @@ from . import build as _build
 ROWWISE = 1
 COLWISE_T = 2
 OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2   # fp8bs_gemm_workspace_bytes products
+DEBUG_F32_OUT = 1                        # fp8bs_debug_set_flags: FP32 accumulator outputs
+_debug_flags = 0
 
 STATUS = {
     0: "FP8BS_OK", 1: "FP8BS_ERR_INVALID_ARG", 2: "FP8BS_ERR_SHAPE", 3: "FP8BS_ERR_ALIGN",
@@ -59,8 +61,11 @@ SIGNATURES = {
     "fp8bs_gemm_wgrad_accumulate_f32": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8bs_launch_count": (_I64, []),
+    "fp8bs_debug_tensor_map_encodes": (_I64, []),
     "fp8bs_debug_set_wait_timeout_ns": (ctypes.c_int, [_I64]),
     "fp8bs_debug_set_fault": (ctypes.c_int, [ctypes.c_int]),
+    "fp8bs_debug_set_flags": (ctypes.c_int, [ctypes.c_uint]),
+    "fp8bs_debug_occupy_sms": (ctypes.c_int, [ctypes.c_int, _I64, _P]),
     "fp8bs_debug_e4m3_encode_bits": (ctypes.c_int, [ctypes.c_uint32, _I64, _P, _P]),
 }
 
@@ -125,6 +130,11 @@ def _out(t: Optional[torch.Tensor], shape, dtype, device) -> torch.Tensor:
     return torch.empty(shape, dtype=dtype, device=device) if t is None else t
 
 
+def _gemm_out_dtype():
+    """BF16, or FP32 while the FP32-output test mode is on."""
+    return torch.float32 if _debug_flags & DEBUG_F32_OUT else torch.bfloat16
+
+
 # ---------------------------------------------------------------- entry points
 
 def padded_tokens(rows: int) -> int:
@@ -183,11 +193,11 @@ def fp8bs_gemm_fprop(xq, sx, wq, sw, y=None, stream=None, split=True) -> torch.T
     N = wq.shape[0]
     if split:
         _ensure_workspace(OP_FPROP, M, N, K, xq.device)
-    y = _out(y, (M, N), torch.bfloat16, xq.device)
+    y = _out(y, (M, N), _gemm_out_dtype(), xq.device)
     _check(load().fp8bs_gemm_fprop(
         _dev(xq, torch.uint8, (M, K), "xq"), _dev(sx, torch.float32, (K // 128, padded_tokens(M)), "sx"),
         _dev(wq, torch.uint8, (N, K), "wq"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
-        _dev(y, torch.bfloat16, (M, N), "y"), M, N, K, _stream(stream)), "fp8bs_gemm_fprop")
+        _dev(y, _gemm_out_dtype(), (M, N), "y"), M, N, K, _stream(stream)), "fp8bs_gemm_fprop")
     return y
 
 
@@ -250,11 +260,11 @@ def fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, dx=None, stream=None, split=True) -> tor
     K = wqT.shape[0]
     if split:
         _ensure_workspace(OP_DGRAD, M, N, K, dyq.device)
-    dx = _out(dx, (M, K), torch.bfloat16, dyq.device)
+    dx = _out(dx, (M, K), _gemm_out_dtype(), dyq.device)
     _check(load().fp8bs_gemm_dgrad(
         _dev(dyq, torch.uint8, (M, N), "dyq"), _dev(sdy, torch.float32, (N // 128, padded_tokens(M)), "sdy"),
         _dev(wqT, torch.uint8, (K, N), "wqT"), _dev(sw, torch.float32, (N // 128, K // 128), "sw"),
-        _dev(dx, torch.bfloat16, (M, K), "dx"), M, N, K, _stream(stream)), "fp8bs_gemm_dgrad")
+        _dev(dx, _gemm_out_dtype(), (M, K), "dx"), M, N, K, _stream(stream)), "fp8bs_gemm_dgrad")
     return dx
 
 
@@ -263,9 +273,13 @@ _workspaces = {}  # device index -> registered scratch tensor
 
 def _ensure_workspace(op: int, M: int, N: int, K: int, device) -> None:
     """Registers (torch-allocated) scratch for the split-K path of product
-    `op` if this shape would use more than the device has registered.  A
-    new buffer replaces the old one only after the device is idle."""
-    need = int(load().fp8bs_gemm_workspace_bytes(op, M, N, K))
+    `op` if this shape would use more than the device has registered."""
+    _ensure_workspace_bytes(int(load().fp8bs_gemm_workspace_bytes(op, M, N, K)), device)
+
+
+def _ensure_workspace_bytes(need: int, device) -> None:
+    """Registers at least `need` bytes of scratch on `device`.  A new buffer
+    replaces the old one only after the device is idle."""
     if need <= 0:
         return
     idx = device.index if device.index is not None else torch.cuda.current_device()
@@ -307,11 +321,11 @@ def fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, dw=None, stream=None, split=True) -> 
     K = xTq.shape[0]
     if split:
         _ensure_workspace(OP_WGRAD, M, N, K, dyTq.device)
-    dw = _out(dw, (N, K), torch.bfloat16, dyTq.device)
+    dw = _out(dw, (N, K), _gemm_out_dtype(), dyTq.device)
     _check(load().fp8bs_gemm_wgrad(
         _dev(dyTq, torch.uint8, (N, M), "dyTq"), _dev(sdyT, torch.float32, (M // 128, N), "sdyT"),
         _dev(xTq, torch.uint8, (K, M), "xTq"), _dev(sxT, torch.float32, (M // 128, K), "sxT"),
-        _dev(dw, torch.bfloat16, (N, K), "dw"), M, N, K, _stream(stream)), "fp8bs_gemm_wgrad")
+        _dev(dw, _gemm_out_dtype(), (N, K), "dw"), M, N, K, _stream(stream)), "fp8bs_gemm_wgrad")
     return dw
 
 
@@ -357,6 +371,15 @@ def fp8bs_debug_set_wait_timeout_ns(ns: int) -> None:
     _check(load().fp8bs_debug_set_wait_timeout_ns(ns), "fp8bs_debug_set_wait_timeout_ns")
 
 
+def fp8bs_debug_set_flags(flags: int) -> None:
+    """Test modes of the GEMMs (DEBUG_F32_OUT: fprop / dgrad / wgrad write
+    their FP32 accumulators; the wrappers then allocate float32 outputs);
+    0 turns them off."""
+    global _debug_flags
+    _check(load().fp8bs_debug_set_flags(flags), "fp8bs_debug_set_flags")
+    _debug_flags = flags
+
+
 def fp8bs_debug_set_fault(mode: int) -> None:
     _check(load().fp8bs_debug_set_fault(mode), "fp8bs_debug_set_fault")
 
@@ -377,17 +400,21 @@ def fp8bs_debug_split_plan(tiles: int, kblocks: int, sms: int) -> dict:
     return {"splits": out[0], "tail_first": out[1], "units": out[2], "bytes": out[3]}
 
 
-def fp8bs_gemm_group(members, stream=None):
+def fp8bs_gemm_group(members, stream=None, split=True):
     """Several products in one launch.  `members` lists (op, a, sa, b, sb,
     out) with op OP_FPROP (a = Xq, sa = sx, b = Wq, sb = sw), OP_DGRAD (dYq,
     sdy, WqT, sw) or OP_WGRAD (dYTq, sdyT, XTq, sxT), operand layouts as for
     that op's own function; `out` may be None (allocated).  Forward and
     data-gradient products may share a group, weight gradients group alone.
-    Returns the outputs in order; each equals the op's unsplit result."""
+    Returns the outputs in order.  With split=True the binding registers
+    scratch for every member's split plan, so each output equals the op's
+    own call (split=True) bit for bit; without scratch each equals the op's
+    unsplit result."""
     if not 1 <= len(members) <= GROUP_MAX:
         raise ValueError(f"a group has 1..{GROUP_MAX} members, got {len(members)}")
     arr = (GemmArgs * len(members))()
     outs = []
+    need = 0
     for i, (op, a, sa, b, sb, out) in enumerate(members):
         if op == OP_FPROP:
             (M, K), N = a.shape, b.shape[0]
@@ -405,6 +432,9 @@ def fp8bs_gemm_group(members, stream=None):
         arr[i] = GemmArgs(op, _dev(a, torch.uint8, shapes[0], "a"), _dev(sa, torch.float32, shapes[1], "sa"),
                           _dev(b, torch.uint8, shapes[2], "b"), _dev(sb, torch.float32, shapes[3], "sb"),
                           _dev(out, torch.bfloat16, shapes[4], "out"), M, N, K)
+        need += max(0, int(load().fp8bs_gemm_workspace_bytes(op, M, N, K)))
         outs.append(out)
+    if split and need > 0:
+        _ensure_workspace_bytes(need, members[0][1].device)
     _check(load().fp8bs_gemm_group(arr, len(members), _stream(stream)), "fp8bs_gemm_group")
     return outs

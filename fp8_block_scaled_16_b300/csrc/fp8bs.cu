@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <unordered_map>
 #include <cstring>
 #include <mutex>
 
@@ -20,12 +21,22 @@ namespace fp8bs {
 // Per-device status word written by kernels that give up a bounded wait.
 __device__ uint32_t g_device_status;
 
-// Scratch of fp8bs_gemm_wgrad_noalloc: split-K flags (first 64 KiB) and FP32
+// Scratch of fp8bs_gemm_wgrad_noalloc: split-K arrival counters (first 64 KiB) and FP32
 // partial sums, in static device memory that exists on every device where
 // this library's kernels are loaded, for the life of the process.  In host
 // code this name is only a handle: its device address comes from
 // cudaGetSymbolAddress.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[FP8BS_NOALLOC_SCRATCH_BYTES];
+
+// Test hook: holds one SM per CTA (its shared memory leaves room for no
+// other CTA of the library's GEMMs) for `ns` nanoseconds, then exits.
+__global__ void occupy_kernel(int64_t ns) {
+    extern __shared__ uint8_t held[];
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < static_cast<uint64_t>(ns)) __nanosleep(2000);
+    if (threadIdx.x == 0) reinterpret_cast<volatile uint8_t*>(held)[0] = 0;
+}
+constexpr int kOccupySmem = 200 * 1024;
 
 namespace {
 
@@ -35,17 +46,19 @@ constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 std::atomic<int64_t> g_launches{0};
 std::atomic<int64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_fault{0};
+std::atomic<unsigned> g_debug_flags{0};
 
 struct DeviceInfo {
     bool ready = false;
     bool arch_ok = false;
     int sm_count = 0;
     uint32_t* status = nullptr;
-    bool gemm_attr_set[2][2][3] = {};  // [scale mode][grouped][epilogue variant]
+    // Kernel attributes set once per variant: [scale mode][grouped][epilogue].
+    std::atomic<bool> gemm_attr_set[2][2][3] = {};
     // Caller-registered scratch for split-K GEMMs (fp8bs_set_workspace).
     uint8_t* ws = nullptr;
     int64_t ws_bytes = 0;
-    std::atomic<uint32_t> epoch{0};
+    std::atomic<uint64_t> epoch{0};  // split-K launch tags (64-bit: never wraps)
     // fp8bs_gemm_wgrad_noalloc: device address of g_noalloc_scratch on this
     // device, looked up by that entry point's first call here.
     bool noalloc_ready = false;
@@ -112,17 +125,61 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return g_encode;
 }
 
+// Cache of encoded TMA tensor maps.  An encoded map is a pure function of
+// its arguments (element type, base address, extents, row stride, box,
+// swizzle), so a cached map is always the one the driver would encode
+// again; the cache only saves the driver call on the launch path.
+struct TmapKey {
+    uint64_t base, inner, outer, row_bytes;
+    uint32_t dt, box_inner, box_outer, sw;
+    bool operator==(const TmapKey& o) const {
+        return base == o.base && inner == o.inner && outer == o.outer && row_bytes == o.row_bytes && dt == o.dt &&
+               box_inner == o.box_inner && box_outer == o.box_outer && sw == o.sw;
+    }
+};
+struct TmapKeyHash {
+    size_t operator()(const TmapKey& k) const {
+        uint64_t h = 1469598103934665603ull;
+        for (uint64_t v : {k.base, k.inner, k.outer, k.row_bytes, uint64_t(k.dt), uint64_t(k.box_inner),
+                           uint64_t(k.box_outer), uint64_t(k.sw)}) {
+            h ^= v;
+            h *= 1099511628211ull;
+        }
+        return static_cast<size_t>(h);
+    }
+};
+constexpr size_t kTmapCacheMax = 4096;  // entries; the cache is emptied when it fills
+std::mutex g_tmap_mu;
+std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmap_cache;
+std::atomic<int64_t> g_tmap_encodes{0};
+
 // 2-D row-major tensor [outer][inner] of `elem` bytes per element.
 bool tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    const TmapKey key{reinterpret_cast<uint64_t>(base), inner, outer, row_bytes, static_cast<uint32_t>(dt),
+                      box_inner, box_outer, static_cast<uint32_t>(sw)};
+    {
+        std::lock_guard<std::mutex> lk(g_tmap_mu);
+        auto it = g_tmap_cache.find(key);
+        if (it != g_tmap_cache.end()) {
+            *m = it->second;
+            return true;
+        }
+    }
     auto fn = encoder();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
-    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    g_tmap_encodes.fetch_add(1);
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    if (g_tmap_cache.size() >= kTmapCacheMax) g_tmap_cache.clear();
+    g_tmap_cache.emplace(key, *m);
+    return true;
 }
 
 int launch_status() {
@@ -136,14 +193,16 @@ int launch_status() {
 //   tail:    the tiles past the last full wave in S parts (S x tail tiles
 //            <= SMs, at least 4 K blocks each), the full waves whole.
 // Plans are compared by estimated time in K-block units (~0.6 us each): a
-// unit adds one block for its set-up and store; a helper's publication of
-// its 128 KB FP32 partial costs ~5 blocks and the owner's read-and-add ~2
+// unit adds one block for its set-up and store; the publication of a part's
+// 128 KB FP32 partial costs ~5 blocks and the last part's read-and-add ~2
 // blocks per partial (both limited by one SM's ~100 GB/s to L2, measured
 // on B300).  A plan is used only if it saves at least 5% over no split, and
-// only while its completion flags fit the fixed flag region.  So short
+// only while its arrival counters fit the fixed counter region.  So short
 // contractions (a forward product with K = 2048) are never split: moving
 // the partials would cost more than the idle SMs of the last wave.
-constexpr int64_t kFlagBytes = 64 * 1024;         // flag region at the start of the scratch
+// Scratch layout: the counters ([split tiles][8 warps] x 8 bytes) in the
+// first kFlagBytes, then one FP32 partial per part of every split tile.
+constexpr int64_t kFlagBytes = 64 * 1024;         // counter region at the start of the scratch
 constexpr int64_t kPartialBytes = 128 * 256 * 4;  // one tile's FP32 partial
 struct SplitPlan {
     int splits;
@@ -159,16 +218,16 @@ SplitPlan plan_splits(int64_t tiles, int64_t kblocks, int sms) {
     double best_t = t_none;
     auto consider = [&](int s, int64_t first, double t) {
         const int64_t split_tiles = tiles - first;
-        if ((s - 1) * split_tiles * gemm::NUM_EPI_WARPS * 4 > kFlagBytes) return;
+        if (split_tiles * gemm::NUM_EPI_WARPS * 8 > kFlagBytes) return;
         if (t < best_t && t <= 0.95 * t_none) {
-            best = {s, first, first + s * split_tiles, kFlagBytes + (s - 1) * split_tiles * kPartialBytes};
+            best = {s, first, first + s * split_tiles, kFlagBytes + s * split_tiles * kPartialBytes};
             best_t = t;
         }
     };
     for (int s = 2; s <= 4; s++) {
         if (kblocks / s < 16) continue;
         const double k = static_cast<double>((kblocks + s - 1) / s);
-        consider(s, 0, waves(tiles * s) * (k + kUnitCost) + kPublishCost + kAddCost * (s - 1));
+        consider(s, 0, waves(tiles * s) * (k + kUnitCost) + kPublishCost + kAddCost * s);
     }
     const int64_t full = (tiles / sms) * sms, tail = tiles - full;
     if (full > 0 && tail > 0) {
@@ -176,7 +235,7 @@ SplitPlan plan_splits(int64_t tiles, int64_t kblocks, int sms) {
             if (s * tail > sms || kblocks / s < 4) continue;
             const double k = static_cast<double>((kblocks + s - 1) / s);
             consider(s, full, static_cast<double>(tiles / sms) * (static_cast<double>(kblocks) + kUnitCost) +
-                                  (k + kUnitCost) + kPublishCost + kAddCost * (s - 1));
+                                  (k + kUnitCost) + kPublishCost + kAddCost * s);
         }
     }
     return best;
@@ -196,6 +255,7 @@ struct GemmSpec {
     int64_t sb_stride_j, sb_stride_b;
     void* out;             // BF16 (or FP32 with out_f32_add); may be null when out_q is set
     bool out_f32_add;
+    bool out_f32_store = false;  // test mode: FP32 out = the unrounded accumulator
     uint8_t* out_q = nullptr;  // forward only: 1x128-quantized output and its scales
     float* out_s = nullptr;
     bool swiglu = false;       // forward of an interleaved gate+up weight: outputs are H = SiLU(gate) * up
@@ -233,7 +293,7 @@ int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap*
     const int64_t ocols = s.swiglu ? s.cols / 2 : s.cols;  // columns of the stored output
     if (!tmap_2d(tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.A, s.kc, s.rows, s.kc, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tmap_2d(tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.B, s.kc, s.cols, s.kc, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !(s.out_f32_add ? tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cbase, ocols, s.rows, ocols * 4, 32, 32,
+        !((s.out_f32_add || s.out_f32_store) ? tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cbase, ocols, s.rows, ocols * 4, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_128B)
                         : tmap_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cbase, ocols, s.rows, ocols * 2, 64, 32,
                                   CU_TENSOR_MAP_SWIZZLE_128B)))
@@ -243,7 +303,7 @@ int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap*
                  CU_TENSOR_MAP_SWIZZLE_128B))
         return FP8BS_ERR_LAUNCH;
     p->out_swiglu = s.swiglu ? 1 : 0;
-    p->out_f32_add = s.out_f32_add ? 1 : 0;
+    p->out_f32_add = s.out_f32_store ? 2 : (s.out_f32_add ? 1 : 0);
     p->out_bf16 = s.out != nullptr ? 1 : 0;
     p->out_q = s.out_q != nullptr ? 1 : 0;
     p->out_s = s.out_s;
@@ -265,7 +325,7 @@ int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap*
     p->splits = 1;
     p->tail_first = 0;
     p->ws = nullptr;
-    p->flags = nullptr;
+    p->arrivals = nullptr;
     p->epoch = 0;
     if (static_cast<int64_t>(p->m_tiles) * p->n_tiles > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
     return FP8BS_OK;
@@ -279,15 +339,37 @@ int launch_group(DeviceInfo* d, const gemm::Group<G>& grp, cudaStream_t st) {
     if (units <= 0) return FP8BS_OK;
     const int grid = static_cast<int>(units < d->sm_count ? units : d->sm_count);
     auto kern = gemm_kernel<SBMODE, 256, G, EPI>;
-    bool& attr = d->gemm_attr_set[SBMODE][G > 1 ? 1 : 0][EPI];
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
-            return launch_status();
-        attr = true;
+    std::atomic<bool>& attr = d->gemm_attr_set[SBMODE][G > 1 ? 1 : 0][EPI];
+    if (!attr.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!attr.load(std::memory_order_relaxed)) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
+                return launch_status();
+            attr.store(true, std::memory_order_release);
+        }
     }
     kern<<<grid, THREADS, T::SMEM_BYTES, st>>>(grp);
     g_launches.fetch_add(1);
     return launch_status();
+}
+
+// Test mode (fp8bs_debug_set_flags): the plain products write their FP32
+// accumulators instead of BF16.
+GemmSpec with_debug_flags(GemmSpec s) {
+    if (g_debug_flags.load() & FP8BS_DEBUG_F32_OUT) s.out_f32_store = true;
+    return s;
+}
+
+// A tag for one split-K launch (never 0: counters start cleared).
+uint64_t next_epoch(DeviceInfo* d) { return d->epoch.fetch_add(1) + 1; }
+
+// Makes member `p` run split plan `sp` with its scratch at `base`.
+void apply_split(gemm::Params* p, const SplitPlan& sp, uint8_t* base, uint64_t epoch) {
+    p->splits = sp.splits;
+    p->tail_first = static_cast<int32_t>(sp.tail_first);
+    p->arrivals = reinterpret_cast<unsigned long long*>(base);
+    p->ws = reinterpret_cast<float*>(base + kFlagBytes);
+    p->epoch = epoch;
 }
 
 // One product, split along K when the registered scratch allows a plan that pays.
@@ -303,14 +385,12 @@ int run_gemm(const GemmSpec& s, cudaStream_t st) {
     p.fault = g_fault.exchange(0);
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     int64_t units = tiles;
-    if (d->ws != nullptr) {
+    // The SwiGLU epilogue pairs two warps of one CTA, which split parts
+    // finishing in different CTAs could not do: those products stay whole.
+    if (d->ws != nullptr && !s.swiglu) {
         const SplitPlan sp = plan_splits(tiles, p.kblocks, d->sm_count);
         if (sp.splits > 1 && sp.bytes <= d->ws_bytes) {
-            p.splits = sp.splits;
-            p.tail_first = static_cast<int32_t>(sp.tail_first);
-            p.flags = reinterpret_cast<uint32_t*>(d->ws);
-            p.ws = reinterpret_cast<float*>(d->ws + kFlagBytes);
-            p.epoch = d->epoch.fetch_add(1) + 1;
+            apply_split(&p, sp, d->ws, next_epoch(d));
             units = sp.units;
         }
     }
@@ -381,7 +461,7 @@ int fp8bs_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, cons
                      int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(xq, sx, wq, sw, y, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    return run_gemm(spec_of(FP8BS_OP_FPROP, xq, sx, wq, sw, y, M, N, K), static_cast<cudaStream_t>(stream));
+    return run_gemm(with_debug_flags(spec_of(FP8BS_OP_FPROP, xq, sx, wq, sw, y, M, N, K)), static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemm_fprop_quant(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, void* y,
@@ -414,14 +494,14 @@ int fp8bs_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, c
                      int64_t M, int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(dyq, sdy, wqT, sw, dx, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    return run_gemm(spec_of(FP8BS_OP_DGRAD, dyq, sdy, wqT, sw, dx, M, N, K), static_cast<cudaStream_t>(stream));
+    return run_gemm(with_debug_flags(spec_of(FP8BS_OP_DGRAD, dyq, sdy, wqT, sw, dx, M, N, K)), static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemm_wgrad(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT, void* dw,
                      int64_t M, int64_t N, int64_t K, void* stream) {
     int rc = check_gemm_args(dyTq, sdyT, xTq, sxT, dw, M, N, K);
     if (rc != FP8BS_OK) return rc;
-    return run_gemm(spec_of(FP8BS_OP_WGRAD, dyTq, sdyT, xTq, sxT, dw, M, N, K), static_cast<cudaStream_t>(stream));
+    return run_gemm(with_debug_flags(spec_of(FP8BS_OP_WGRAD, dyTq, sdyT, xTq, sxT, dw, M, N, K)), static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, const uint8_t* xTq, const float* sxT,
@@ -453,12 +533,25 @@ int fp8bs_gemm_group(const fp8bs_gemm_args* gemms, int count, void* stream) {
     Group<kGroupMax> grp;
     grp.count = count;
     grp.first_unit[0] = 0;
+    // Each member may split as it would alone, in its own region of the
+    // registered scratch (members that no longer fit stay whole).
+    int64_t ws_used = 0;
+    const uint64_t epoch = d->ws != nullptr ? next_epoch(d) : 0;
     for (int i = 0; i < count; i++) {
         const fp8bs_gemm_args& a = gemms[i];
         rc = fill_member(d, spec_of(a.op, a.a, a.sa, a.b, a.sb, a.out, a.M, a.N, a.K), &grp.tmA[i], &grp.tmB[i],
                          &grp.tmC[i], &grp.tmQ[i], &grp.p[i]);
         if (rc != FP8BS_OK) return rc;
-        const int64_t end = grp.first_unit[i] + static_cast<int64_t>(grp.p[i].m_tiles) * grp.p[i].n_tiles;
+        int64_t member_units = static_cast<int64_t>(grp.p[i].m_tiles) * grp.p[i].n_tiles;
+        if (d->ws != nullptr) {
+            const SplitPlan sp = plan_splits(member_units, grp.p[i].kblocks, d->sm_count);
+            if (sp.splits > 1 && ws_used + sp.bytes <= d->ws_bytes) {
+                apply_split(&grp.p[i], sp, d->ws + ws_used, epoch);
+                ws_used += sp.bytes;
+                member_units = sp.units;
+            }
+        }
+        const int64_t end = grp.first_unit[i] + member_units;
         if (end > (int64_t(1) << 30)) return FP8BS_ERR_SHAPE;
         grp.first_unit[i + 1] = static_cast<int32_t>(end);
     }
@@ -545,18 +638,10 @@ int fp8bs_gemm_wgrad_noalloc(const uint8_t* dyTq, const float* sdyT, const uint8
                      &grp.tmC[0], &grp.tmQ[0], &p);
     if (rc != FP8BS_OK) return rc;
     if (sp.splits > 1) {
-        // The scratch keeps whatever the previous call left: clear the flags
-        // this call will use (partials are always written before they are read).
-        const int64_t flag_bytes = (sp.splits - 1) * (tiles - sp.tail_first) * NUM_EPI_WARPS * 4;
-        if (cudaMemsetAsync(d->noalloc_scratch, 0, static_cast<size_t>(flag_bytes), st) != cudaSuccess) {
-            cudaGetLastError();
-            return FP8BS_ERR_LAUNCH;
-        }
-        p.splits = sp.splits;
-        p.tail_first = static_cast<int32_t>(sp.tail_first);
-        p.flags = reinterpret_cast<uint32_t*>(d->noalloc_scratch);
-        p.ws = reinterpret_cast<float*>(d->noalloc_scratch + kFlagBytes);
-        p.epoch = 1;
+        // The array keeps whatever the previous call left; the arrival
+        // counters carry this call's own tag, so nothing needs clearing
+        // (partials are always written before they are read).
+        apply_split(&p, sp, d->noalloc_scratch, next_epoch(d));
     }
     grp.count = 1;
     grp.first_unit[0] = 0;
@@ -597,6 +682,8 @@ const char* fp8bs_status_string(int status) {
 
 int64_t fp8bs_launch_count(void) { return g_launches.load(); }
 
+int64_t fp8bs_debug_tensor_map_encodes(void) { return g_tmap_encodes.load(); }
+
 int fp8bs_debug_set_wait_timeout_ns(int64_t ns) {
     if (ns < 0) return FP8BS_ERR_INVALID_ARG;
     g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
@@ -612,6 +699,25 @@ int fp8bs_debug_split_plan(int64_t tiles, int64_t kblocks, int sms, int64_t* out
     out[1] = sp.tail_first;
     out[2] = sp.units;
     out[3] = sp.bytes;
+    return FP8BS_OK;
+}
+
+int fp8bs_debug_occupy_sms(int ctas, int64_t ns, void* stream) {
+    if (ctas < 1 || ns < 0 || ns > 2000000000LL) return FP8BS_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK) return rc;
+    if (ctas > d->sm_count) return FP8BS_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kOccupySmem) != cudaSuccess)
+        return launch_status();
+    occupy_kernel<<<ctas, 32, kOccupySmem, static_cast<cudaStream_t>(stream)>>>(ns);
+    g_launches.fetch_add(1);
+    return launch_status();
+}
+
+int fp8bs_debug_set_flags(unsigned flags) {
+    if (flags & ~static_cast<unsigned>(FP8BS_DEBUG_F32_OUT)) return FP8BS_ERR_INVALID_ARG;
+    g_debug_flags.store(flags);
     return FP8BS_OK;
 }
 

@@ -154,7 +154,8 @@ struct Params {
     uint32_t* status;
     uint64_t timeout_ns;
     int32_t fault;                // test hook: withhold CTA 0's first operand copy
-    int32_t out_f32_add;          // 0: BF16 store into out; 1: FP32 out += result (tmC is FP32)
+    int32_t out_f32_add;          // 0: BF16 store into out; 1: FP32 out += result; 2: FP32 out = result
+                                  // (test mode: the unrounded accumulator); tmC is FP32 for 1 and 2
     int32_t out_bf16;             // store the BF16 output (tmC); 0 only with out_q
     // Forward product only: the BF16-rounded output also quantized in 1x128
     // row tiles -- E4M3 payload [rows][cols] through tmQ, FP32 scales
@@ -169,23 +170,24 @@ struct Params {
     // through tmQ / out_s, both [rows][cols/2].
     int32_t out_swiglu;
     // K splits (1 = none) of the tiles t >= tail_first (0: of every tile).
-    // With T = tiles - tail_first split tiles, split s > 0 of tile t is a
-    // helper that leaves its FP32 partial in ws slot (s-1)*T + (t-tail_first)
-    // and sets flags[slot*8 + warp] = epoch; split 0 is the owner that adds
-    // the helpers' partials, in split order, before it stores the tile.
+    // With T = tiles - tail_first split tiles, each part s of tile t leaves
+    // its FP32 partial in ws slot (t - tail_first) * splits + s and then
+    // counts itself in arrivals[(t - tail_first) * 8 + warp]; the part that
+    // arrives last adds all the partials in part order and stores the
+    // tile's slice.  No part waits for another, so the parts need not be
+    // resident at the same time.  A counter holds (epoch << 8) | arrivals;
+    // a value with another epoch counts as zero, so counters left by
+    // earlier launches need no clearing.
     int32_t splits;
     int32_t tail_first;
-    float* ws;                    // [(splits-1)*T][8 warps][32 float4][32 lanes]
-    uint32_t* flags;              // [(splits-1)*T][8]
-    uint32_t epoch;
+    float* ws;                    // [T * splits][8 warps][32 float4][32 lanes]
+    unsigned long long* arrivals; // [T][8]
+    unsigned long long epoch;     // unique per launch, never 0
 };
 
-// One unit of work: K blocks [kb0, kb1) of output tile t, split s (split:
+// One unit of work: K blocks [kb0, kb1) of output tile t, part s (split:
 // the tile is computed in parts).  Units are numbered whole tiles first
-// (t < tail_first), then the helpers (s > 0) of the split tiles, then their
-// owners (s == 0), so a CTA, which takes its units in increasing order, has
-// finished all of its whole-tile and helper units before it can wait on
-// anyone; those never wait.
+// (t < tail_first), then part 0 of every split tile, then part 1, ...
 struct Unit {
     int t, s, kb0, kb1;
     bool split;
@@ -204,13 +206,8 @@ __device__ __forceinline__ Unit unit_of(int u, const Params& p, int num_tiles) {
         return w;
     }
     const int v = u - p.tail_first, nt = num_tiles - p.tail_first;
-    const int helpers = (p.splits - 1) * nt;
-    if (v < helpers) {
-        w.s = 1 + v / nt;
-        w.t = p.tail_first + v - (w.s - 1) * nt;
-    } else {
-        w.t = p.tail_first + v - helpers;
-    }
+    w.s = v / nt;
+    w.t = p.tail_first + v - w.s * nt;
     w.split = p.splits > 1;
     w.kb0 = static_cast<int>(static_cast<int64_t>(w.s) * p.kblocks / p.splits);
     w.kb1 = static_cast<int>(static_cast<int64_t>(w.s + 1) * p.kblocks / p.splits);
@@ -240,22 +237,26 @@ __device__ __forceinline__ int member_of(const Group<G>& grp, int u) {
     return g;
 }
 
-// Waits (bounded) until a helper's flag carries this launch's epoch.
-__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, const WaitCtx& w) {
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        uint32_t v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v == epoch) return true;
-        if (*w.abort_flag) return false;
-        if (global_timer_ns() - t0 > w.timeout_ns) {
-            *w.abort_flag = 1u;
-            atomicOr(w.status, kStatusTimeout);
-            __threadfence();
-            return false;
-        }
-        __nanosleep(64);
+// Counts one part of a split tile as arrived and returns the arrivals so
+// far, this one included (0 on a failed update, with the CTA's abort flag
+// and the device status set).  The counter holds (epoch << 8) | arrivals; a
+// value with another epoch is a leftover of an earlier launch and counts as
+// zero.  Lock-free: a failed compare-and-swap means another part's update
+// succeeded, so with at most 8 parts the loop ends within 8 retries (the cap
+// only guards against a corrupted counter).
+__device__ __forceinline__ uint32_t count_arrival(unsigned long long* ctr, unsigned long long epoch,
+                                                  const WaitCtx& w) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    for (int tries = 0; tries < 64; tries++) {
+        const unsigned long long next = (cur >> 8) == epoch ? cur + 1 : (epoch << 8) | 1ull;
+        const unsigned long long got = atomicCAS(ctr, cur, next);
+        if (got == cur) return static_cast<uint32_t>(next & 0xFFull);
+        cur = got;
     }
+    *w.abort_flag = 1u;
+    atomicOr(w.status, kStatusTimeout);
+    __threadfence();
+    return 0u;
 }
 
 // Bounded wait for the warps on the hand-off path, without a warp vote:
@@ -655,30 +656,37 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             }
             if (!ok) break;
             if (w.split) {
-                const int nt = num_tiles - p.tail_first;
-                if (w.s > 0) {
-                    // Helper: publish this warp's FP32 partial (lane-interleaved float4s,
-                    // so every store instruction writes 512 contiguous bytes), then the flag.
-                    const int slot_id = (w.s - 1) * nt + (w.t - p.tail_first);
-                    float4* dst = reinterpret_cast<float4*>(p.ws) + (static_cast<int64_t>(slot_id) * NUM_EPI_WARPS + ew) * 1024;
+                // Publish this warp's FP32 partial (lane-interleaved float4s, so
+                // every store instruction writes 512 contiguous bytes), then count
+                // it; the part that arrives last finishes the slice.
+                const int64_t tile_id = w.t - p.tail_first;
+                const float4* part0 = reinterpret_cast<const float4*>(p.ws) +
+                                      (tile_id * p.splits * NUM_EPI_WARPS + ew) * 1024;
+                float4* dst = reinterpret_cast<float4*>(p.ws) +
+                              ((tile_id * p.splits + w.s) * NUM_EPI_WARPS + ew) * 1024;
 #pragma unroll
-                    for (int c = 0; c < 32; c++)
-                        dst[c * 32 + lane] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0)
-                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + slot_id * NUM_EPI_WARPS + ew),
-                                     "r"(p.epoch)
-                                     : "memory");
-                    continue;
+                for (int c = 0; c < 32; c++)
+                    dst[c * 32 + lane] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+                __threadfence();
+                __syncwarp();
+                uint32_t arrived = 0;
+                if (lane == 0) arrived = count_arrival(p.arrivals + tile_id * NUM_EPI_WARPS + ew, p.epoch, wc);
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == 0u) { ok = false; break; }
+                if (arrived != static_cast<uint32_t>(p.splits)) continue;
+                // Last part: every partial is published.  Sum them in part order
+                // (this part's own included, as published), whichever CTA this is.
+                __threadfence();
+#pragma unroll
+                for (int c = 0; c < 32; c++) {
+                    const float4 v = __ldcg(part0 + c * 32 + lane);
+                    acc[4 * c] = v.x;
+                    acc[4 * c + 1] = v.y;
+                    acc[4 * c + 2] = v.z;
+                    acc[4 * c + 3] = v.w;
                 }
-                // Owner: add the helpers' partials in split order.
-                for (int j = 1; ok && j < p.splits; j++) {
-                    const int slot_id = (j - 1) * nt + (w.t - p.tail_first);
-                    const bool got = wait_flag(p.flags + slot_id * NUM_EPI_WARPS + ew, p.epoch, wc);
-                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                    const float4* src =
-                        reinterpret_cast<const float4*>(p.ws) + (static_cast<int64_t>(slot_id) * NUM_EPI_WARPS + ew) * 1024;
+                for (int j = 1; j < p.splits; j++) {
+                    const float4* src = part0 + static_cast<int64_t>(j) * NUM_EPI_WARPS * 1024;
 #pragma unroll
                     for (int c = 0; c < 32; c++) {
                         const float4 v = __ldcg(src + c * 32 + lane);
@@ -688,7 +696,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                         acc[4 * c + 3] += v.w;
                     }
                 }
-                if (!ok) break;
             }
             if constexpr (SBMODE == SB_SCALAR) {
                 if constexpr (EPI == EPI_SWIGLU) {
@@ -848,8 +855,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                     __syncwarp();
                     if (lane == 0) {
                         const int32_t x0 = nb * BN + half * COLS + h * 64, y0 = mb * BM + quad * 32;
-                        tma_reduce_add_2d(&grp.tmC[g], stage_out, x0, y0);
-                        tma_reduce_add_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, x0 + 32, y0);
+                        if (p.out_f32_add == 2) {
+                            tma_store_2d(&grp.tmC[g], stage_out, x0, y0);
+                            tma_store_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, x0 + 32, y0);
+                        } else {
+                            tma_reduce_add_2d(&grp.tmC[g], stage_out, x0, y0);
+                            tma_reduce_add_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, x0 + 32, y0);
+                        }
                         bulk_commit_group();
                     }
                 }

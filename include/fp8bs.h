@@ -25,6 +25,10 @@
  *     (128x1 tiles) from their BF16 originals and stored transposed, so the
  *     token dimension becomes the contraction dimension.
  *
+ * Library state: a per-device status word, per-device split-K scratch
+ * registration, and a cache of encoded TMA tensor maps (keyed by pointer
+ * and shape; an entry is exactly what re-encoding would produce).
+ *
  * Conventions for every entry point:
  *   - All tensors are row-major and contiguous; "[a][b]" means a rows of b.
  *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
@@ -61,7 +65,7 @@ typedef enum fp8bs_status {
     FP8BS_ERR_INVALID_ARG = 1, /* a required pointer is NULL, or bad flags */
     FP8BS_ERR_SHAPE = 2,       /* a dimension is <= 0, not a multiple of 128, or too large */
     FP8BS_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
-    FP8BS_ERR_ARCH = 4,        /* no CUDA device, or the device is not sm_103 / sm_100 family */
+    FP8BS_ERR_ARCH = 4,        /* no CUDA device, or the current device is not compute capability 10.3 (sm_103) */
     FP8BS_ERR_LAUNCH = 5,      /* the CUDA runtime reported an error at launch */
     FP8BS_ERR_TIMEOUT = 6,     /* a bounded wait inside a kernel expired (device status) */
     FP8BS_ERR_CUDA = 7         /* a CUDA runtime call failed (device status query) */
@@ -225,9 +229,12 @@ int fp8bs_gemm_wgrad_accumulate_f32(const uint8_t* dyTq, const float* sdyT, cons
  *                  sxT, out = y / dx / dw as BF16).  Forward and data-gradient
  *                  products may share a group; weight gradients form groups
  *                  of their own (their promotion differs).
- * Each output is bitwise equal to the unsplit result of the member's own
- * entry point (no split-K inside a group).  Outputs must not overlap each
- * other or any input.  Errors: FP8BS_ERR_INVALID_ARG for a NULL array, a
+ * With registered scratch (fp8bs_set_workspace) large enough for every
+ * member's split plan, each member splits as its own entry point would, in
+ * its own region of the scratch (regions in member order; a member that no
+ * longer fits stays whole), and each output is bitwise equal to the
+ * member's own call; without scratch, to its unsplit result.  Outputs must
+ * not overlap each other or any input.  Errors: FP8BS_ERR_INVALID_ARG for a NULL array, a
  * count out of range, an unknown op or mixed weight-gradient and other
  * members; otherwise as for the members' entry points (checked before
  * anything is launched).
@@ -252,9 +259,12 @@ int fp8bs_gemm_group(const fp8bs_gemm_args* gemms, int count, void* stream);
  * FP32 partial sums (a weight gradient over many tokens with few tiles, e.g.
  * 2048 x 5632 outputs), the contraction of the last wave's tiles, or of all
  * tiles, is split into 2-8 parts computed by different CTAs.  Each part
- * keeps the per-128-K promotion chain; the parts' FP32 partial sums are
- * added in a fixed order (part 0 + part 1 + ...), so results stay bitwise
- * deterministic.  The partial sums go through this scratch buffer:
+ * keeps the per-128-K promotion chain over its own K blocks and publishes
+ * its FP32 partial sum; whichever part finishes last adds all of them in a
+ * fixed order (part 0 + part 1 + ...), so results stay bitwise
+ * deterministic, and no CTA ever waits for another (the parts need not be
+ * resident at the same time).  Forward products with the SwiGLU epilogue
+ * are not split.  The partial sums go through this scratch buffer:
  *
  *   fp8bs_gemm_workspace_bytes(op, M, N, K): bytes the current device needs
  *     for product `op` (FP8BS_OP_FPROP, _DGRAD, _WGRAD) with the arguments
@@ -264,7 +274,7 @@ int fp8bs_gemm_group(const fp8bs_gemm_args* gemms, int count, void* stream);
  *   fp8bs_set_workspace(ws, bytes): registers `bytes` of DEVICE memory at
  *     `ws` (256-byte aligned, bytes >= 64 KiB; NULL and 0 unregister) as the
  *     current device's scratch.  The library zeroes its first 64 KiB (the
- *     completion flags) with a blocking cudaMemset and keeps the pointer; the
+ *     arrival counters) with a blocking cudaMemset and keeps the pointer; the
  *     caller keeps the memory alive and unmodified while it is registered,
  *     and registers only while no GEMM is running.  Without a large enough
  *     registration a product simply does not split.  GEMMs that share one
@@ -297,10 +307,11 @@ int64_t fp8bs_gemm_wgrad_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   - Shapes whose split plan needs more scratch than the array holds are
  *     rejected with FP8BS_ERR_SHAPE before anything is launched
  *     (fp8bs_gemm_wgrad_workspace_bytes tells the need).
- *   - Every call on a device shares the one array; each call first clears
- *     (cudaMemsetAsync on `stream`) the completion flags it will use.  Two
- *     calls that may overlap on the GPU (different streams, no ordering
- *     between them) race on the array and give wrong results.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; each call tags its arrival counters with its own
+ *     number, so nothing needs clearing first.  Two calls that may overlap
+ *     on the GPU (different streams, no ordering between them) race on the
+ *     array and give wrong results.
  *   - Errors as for fp8bs_gemm_wgrad; FP8BS_ERR_CUDA if the array's address
  *     cannot be looked up.
  */
@@ -321,6 +332,12 @@ const char* fp8bs_status_string(int status);
  * entry points, all devices); a diagnostic counter. */
 int64_t fp8bs_launch_count(void);
 
+/* Number of TMA tensor maps the library has encoded with the driver.  The
+ * GEMM entry points keep encoded maps in a cache keyed by pointer, shape,
+ * stride, box and swizzle (an encoded map depends on nothing else), so a
+ * repeated call on the same buffers encodes none; a diagnostic counter. */
+int64_t fp8bs_debug_tensor_map_encodes(void);
+
 /*
  * Test hooks (not for production use).
  *   fp8bs_debug_set_wait_timeout_ns: the limit of every bounded device wait
@@ -334,6 +351,17 @@ int64_t fp8bs_launch_count(void);
  *   fp8bs_debug_silu_mul: h[i] = bf16(SiLU(g[i]) * u[i]) on BF16 bit patterns
  *     (device arrays of n elements), the activation of
  *     fp8bs_gemm_fprop_swiglu_quant.
+ *   fp8bs_debug_set_flags: test modes of the GEMMs, until reset with 0.
+ *     FP8BS_DEBUG_F32_OUT: fp8bs_gemm_fprop, _dgrad and _wgrad write the FP32
+ *     promotion accumulator itself -- float [rows][cols], 4 bytes per
+ *     element in the same output pointer -- instead of its BF16 rounding, so
+ *     that a test can compare the tensor-core partial sums and the promotion
+ *     chain with a reference without the BF16 step.  Other entry points
+ *     ignore it.  FP8BS_ERR_INVALID_ARG for unknown bits.
+ *   fp8bs_debug_occupy_sms: launches `ctas` (1 .. SM count) CTAs on `stream`
+ *     that each hold one SM -- their shared memory leaves no room for a GEMM
+ *     CTA -- for `ns` nanoseconds (at most 2e9), then exit: for testing that
+ *     a GEMM on another stream completes while part of the GPU is busy.
  *   fp8bs_debug_split_plan: the split-K plan for `tiles` output tiles of
  *     `kblocks` 128-wide contraction blocks on `sms` SMs, host only (no
  *     device needed): out[0] splits (1 = none), out[1] the first split tile
@@ -341,6 +369,9 @@ int64_t fp8bs_launch_count(void);
  *     FP8BS_ERR_INVALID_ARG for non-positive sizes or a NULL `out`.
  */
 int fp8bs_debug_set_wait_timeout_ns(int64_t ns);
+#define FP8BS_DEBUG_F32_OUT 1u
+int fp8bs_debug_set_flags(unsigned flags);
+int fp8bs_debug_occupy_sms(int ctas, int64_t ns, void* stream);
 int fp8bs_debug_set_fault(int mode);
 int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
 int fp8bs_debug_split_plan(int64_t tiles, int64_t kblocks, int sms, int64_t* out);

@@ -399,5 +399,92 @@ def test_long_contraction_full_output():
     _, _, dyTq, sdyT = B.fp8bs_quantize_act(dyt.cuda(), B.COLWISE_T)
     dw = B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT)
     assert B.fp8bs_get_device_status() == 0
-    acc, _, sab = oracle_gemm_rows("wgrad", np_u8(dyTq), np_f32(sdyT), np_u8(xTq), np_f32(sxT), np.arange(Nt))
+    # The 65536-token transposed operands bit for bit, then the oracle's GEMM
+    # on its own quantization.
+    oxTq, osxT = oracle.quant_colwise_128x1_T(xt)
+    odyTq, osdyT = oracle.quant_colwise_128x1_T(dyt)
+    same_bits(xTq, oxTq, "XTq over 65536 tokens")
+    same_bits(sxT, osxT, "sXT over 65536 tokens")
+    same_bits(dyTq, odyTq, "dYTq over 65536 tokens")
+    same_bits(sdyT, osdyT, "sdYT over 65536 tokens")
+    acc, _, sab = oracle_gemm_rows("wgrad", odyTq, osdyT, oxTq, osxT, np.arange(Nt))
     assert_gemm_close(np_bf16_bits(dw), acc, sab, "wgrad over 65536 tokens")
+
+
+def test_tensor_map_cache_reuses_encoded_maps():
+    """A repeated GEMM call on the same buffers takes every TMA tensor map
+    from the cache (no driver encode) and gives the same bits; new buffers
+    are encoded."""
+    M, N, K = 512, 512, 512
+    x = inputs.random_bf16((M, K), seed=71)
+    w = inputs.random_bf16((N, K), seed=72, std=0.02)
+    xq, sx, _, _ = B.fp8bs_quantize_act(x.cuda(), B.ROWWISE)
+    wq, _, sw = B.fp8bs_quantize_weight(w.cuda(), want_t=False)
+    y1 = B.fp8bs_gemm_fprop(xq, sx, wq, sw)
+    e1 = B.load().fp8bs_debug_tensor_map_encodes()
+    y2 = torch.empty_like(y1)
+    B.fp8bs_gemm_fprop(xq, sx, wq, sw, y=y2)
+    e2 = B.load().fp8bs_debug_tensor_map_encodes()
+    B.fp8bs_gemm_fprop(xq, sx, wq, sw, y=y2)
+    assert B.load().fp8bs_debug_tensor_map_encodes() == e2   # all maps cached
+    assert e2 - e1 == 1                                        # only y2's store map was new
+    assert B.fp8bs_get_device_status() == 0
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_split_wgrad_completes_while_other_work_holds_most_sms():
+    """The parts of a split tile never wait for each other: with 100 SMs held
+    for 0.5 s by another stream's kernel, so that most of the GEMM's CTAs
+    start only afterwards, and the device wait limit cut to 0.1 s, a split
+    weight gradient still completes with FP8BS_OK and the same bits as an
+    undisturbed run (a part that waited for a part not yet resident would
+    hit the limit)."""
+    M, N, K = 8192, 2048, 5632
+    assert B.fp8bs_gemm_wgrad_workspace_bytes(M, N, K) > 0, "this shape should split"
+    x = inputs.random_bf16((M, K), seed=141)
+    dy = inputs.random_bf16((M, N), seed=142, std=1e-3)
+    _, _, xTq, sxT = B.fp8bs_quantize_act(x.cuda(), B.COLWISE_T)
+    _, _, dyTq, sdyT = B.fp8bs_quantize_act(dy.cuda(), B.COLWISE_T)
+    ref = B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT)
+    assert B.fp8bs_get_device_status() == 0
+    lib = B.load()
+    busy, work = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    try:
+        assert lib.fp8bs_debug_set_wait_timeout_ns(100_000_000) == 0
+        assert lib.fp8bs_debug_occupy_sms(100, 500_000_000, busy.cuda_stream) == 0
+        with torch.cuda.stream(work):
+            out = B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, stream=work)
+        assert B.fp8bs_get_device_status(work) == 0
+        torch.cuda.synchronize()
+    finally:
+        lib.fp8bs_debug_set_wait_timeout_ns(0)
+    assert B.fp8bs_get_device_status() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_grouped_weight_gradients_split_like_single_calls():
+    """Weight gradients that split on their own split the same way inside a
+    group (each in its own region of the scratch): every output equals the
+    member's own split call bit for bit, and meets the rule on sampled rows."""
+    shapes = [(8192, 2048, 5632), (8192, 256, 512), (2048, 384, 256)]   # (tokens, N, K): tail split, uniform, whole
+    members, singles, data = [], [], []
+    for i, (M, N, K) in enumerate(shapes):
+        x = inputs.random_bf16((M, K), seed=150 + i)
+        dy = inputs.random_bf16((M, N), seed=160 + i, std=1e-3)
+        _, _, xTq, sxT = B.fp8bs_quantize_act(x.cuda(), B.COLWISE_T)
+        _, _, dyTq, sdyT = B.fp8bs_quantize_act(dy.cuda(), B.COLWISE_T)
+        members.append((B.OP_WGRAD, dyTq, sdyT, xTq, sxT, None))
+        data.append((x, dy))
+    assert B.fp8bs_gemm_wgrad_workspace_bytes(*shapes[0]) > 0 and B.fp8bs_gemm_wgrad_workspace_bytes(*shapes[1]) > 0
+    got = B.fp8bs_gemm_group(members)
+    for (_, dyTq, sdyT, xTq, sxT, _) in members:
+        singles.append(B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT))
+    assert B.fp8bs_get_device_status() == 0
+    for g, s1 in zip(got, singles):
+        assert torch.equal(g.view(torch.int16), s1.view(torch.int16))
+    x, dy = data[1]
+    oxTq, osxT = oracle.quant_colwise_128x1_T(x)
+    odyTq, osdyT = oracle.quant_colwise_128x1_T(dy)
+    acc, _, sab = oracle_gemm_rows("wgrad", odyTq, osdyT, oxTq, osxT, np.arange(256))
+    assert_gemm_close(np_bf16_bits(got[1]), acc, sab, "grouped split wgrad")

@@ -27,17 +27,18 @@ def test_short_contraction_is_not_split():
     """Attention QKV forward at 8192 tokens: 64 x 12 = 768 tiles = 5 full
     waves + 28 tiles of 16 K blocks.  Splitting the 28 would save at most
     12 blocks of the last wave, less than moving their FP32 partials costs
-    (a helper's publication ~5 blocks, ~2 per partial for the owner)."""
+    (each part's publication ~5 blocks, ~2 per partial for the last part's sum)."""
     p = plan(tiles_of(8192, 3072), 2048 // 128)
     assert p == {"splits": 1, "tail_first": 0, "units": 768, "bytes": 0}
 
 
 def test_long_contraction_tail_is_split():
     """The same 768 tiles with a 64-block contraction: the 28 tiles past the
-    5 full waves are split in 5 parts (5 x 28 = 140 units <= 148 SMs)."""
+    5 full waves are split in 5 parts (5 x 28 = 140 units <= 148 SMs); every
+    part publishes its partial (5 per split tile)."""
     p = plan(768, 64)
     assert p == {"splits": 5, "tail_first": 740, "units": 740 + 5 * 28,
-                 "bytes": FLAG_BYTES + 4 * 28 * PARTIAL_BYTES}
+                 "bytes": FLAG_BYTES + 5 * 28 * PARTIAL_BYTES}
 
 
 @pytest.mark.parametrize("rows,cols,kblocks,splits,first", [
@@ -78,20 +79,19 @@ def test_plan_invariants_over_a_sweep(sms):
                 continue
             split_tiles = tiles - first
             assert 0 <= first < tiles and units == first + s * split_tiles
-            assert p["bytes"] == FLAG_BYTES + (s - 1) * split_tiles * PARTIAL_BYTES
-            assert (s - 1) * split_tiles * 8 * 4 <= FLAG_BYTES
+            assert p["bytes"] == FLAG_BYTES + s * split_tiles * PARTIAL_BYTES
+            assert split_tiles * 8 * 8 <= FLAG_BYTES   # one 8-byte arrival counter per tile slice
             if first == 0:
                 assert 2 <= s <= 4 and kblocks // s >= 16
             else:
                 assert first % sms == 0 and s * split_tiles <= sms and kblocks // s >= 4
             # The split schedule is really shorter: simulate both.
-            # Units in the kernel's order: whole tiles, then the helpers
-            # (parts 1..s-1) of the split tiles, then their owners (part 0).
+            # Units in the kernel's order: whole tiles, then part 0 of the
+            # split tiles, part 1, ...
             parts = [(j * kblocks) // s for j in range(s + 1)]
             lens = [kblocks] * first
-            for j in range(1, s):
+            for j in range(s):
                 lens += [parts[j + 1] - parts[j]] * split_tiles
-            lens += [parts[1] - parts[0]] * split_tiles
             assert wave_time(lens, sms) < wave_time([kblocks] * tiles, sms)
 
 
