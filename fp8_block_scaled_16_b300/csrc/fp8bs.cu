@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <unordered_map>
@@ -283,6 +284,36 @@ GemmSpec spec_of(int op, const uint8_t* a, const float* sa, const uint8_t* b, co
     }
 }
 
+// Width (in tiles) of the column strips the persistent CTAs take their tiles
+// in.  The tiles running at once -- about one per SM -- are a block of
+// ceil(sms / c) rows by c columns when a strip holds that many tiles, else
+// all m_tiles rows of ceil(sms / m_tiles) columns; they read that many A
+// panels (128 rows x kc bytes) and B panels (256 rows x kc bytes).  The
+// width with the fewest panel bytes per wave is used (row-major, c =
+// n_tiles, on a tie): for the weight gradient of a 2048 x 5632 linear over
+// 32768 tokens (B panels of 8 MB) a row-major wave touches 7 A and 22 B
+// panels (204 MB), one in strips of 10 columns 15 and 10 (140 MB).
+int32_t strip_width(int64_t m_tiles, int64_t n_tiles, int64_t kc, int sms) {
+    int64_t best_c = n_tiles;
+    double best = 0.0;
+    for (int64_t c = n_tiles; c >= 1; c--) {
+        int64_t rows, cols;
+        if (m_tiles * c >= sms) {
+            rows = (sms + c - 1) / c;
+            cols = c;
+        } else {
+            rows = m_tiles;
+            cols = std::min<int64_t>(n_tiles, (sms + m_tiles - 1) / m_tiles);
+        }
+        const double bytes = static_cast<double>(rows) * gemm::BM * kc + static_cast<double>(cols) * 256 * kc;
+        if (c == n_tiles || bytes < best) {
+            best = bytes;
+            best_c = c;
+        }
+    }
+    return static_cast<int32_t>(best_c);
+}
+
 // Tensor maps and kernel parameters of one product, not split.
 int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmC,
                 CUtensorMap* tmQ, gemm::Params* p) {
@@ -311,6 +342,7 @@ int fill_member(DeviceInfo* d, const GemmSpec& s, CUtensorMap* tmA, CUtensorMap*
     p->sa_ld = padded_tokens(s.rows);
     p->n_tiles = static_cast<int32_t>((s.cols + BN - 1) / BN);
     p->kblocks = static_cast<int32_t>(s.kc / BK);
+    p->strip = strip_width(p->m_tiles, p->n_tiles, s.kc, d->sm_count);
     p->nb_valid = static_cast<int32_t>(s.cols / 128);
     p->rows = s.rows;
     p->cols = s.cols;

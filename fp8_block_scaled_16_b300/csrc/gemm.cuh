@@ -143,6 +143,10 @@ struct Tile {
 
 struct Params {
     int32_t m_tiles, n_tiles, kblocks;
+    // Tile order: column strips `strip` tiles wide, row-major inside a strip
+    // (strip == n_tiles: plain row-major), chosen by the host so that the
+    // tiles running at once touch few distinct A and B panels.
+    int32_t strip;
     int32_t nb_valid;             // number of 128-column blocks of the output (cols / 128)
     int64_t rows, cols;           // output shape (rows need not be a multiple of 128)
     int64_t sa_ld;                // row-scale leading dimension: rows rounded up to 128
@@ -212,6 +216,15 @@ __device__ __forceinline__ Unit unit_of(int u, const Params& p, int num_tiles) {
     w.kb0 = static_cast<int>(static_cast<int64_t>(w.s) * p.kblocks / p.splits);
     w.kb1 = static_cast<int>(static_cast<int64_t>(w.s + 1) * p.kblocks / p.splits);
     return w;
+}
+
+// Output tile t's row and column block under the strip order of Params::strip.
+__device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
+    const int per_strip = p.m_tiles * p.strip;
+    const int strip = t / per_strip, local = t - strip * per_strip;
+    const int width = min(p.strip, p.n_tiles - strip * p.strip);
+    mb = local / width;
+    nb = strip * p.strip + (local - mb * width);
 }
 
 // Up to G products computed by one persistent launch: member g owns the
@@ -427,7 +440,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
-            const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
+            int mb, nb;
+            tile_coords(w.t, p, mb, nb);
             for (int kb = w.kb0; kb < w.kb1; kb++) {
                 if (!warp_wait_bounded(bar(T::empty(stage)), ph ^ 1u, wc)) { ok = false; break; }
                 const bool inject = p0.fault != 0 && blockIdx.x == 0 && u == static_cast<int>(blockIdx.x) && kb == w.kb0;
@@ -499,7 +513,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         const uint32_t ring = sbase + T::OFF_SCALE;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
-            const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
+            int mb, nb;
+            tile_coords(w.t, p, mb, nb);
             // One slot per K block (weight gradient) or per SBATCH K blocks.
             constexpr int step = SBMODE == SB_SCALAR ? T::SBATCH : 1;
             for (int kb = w.kb0; kb < w.kb1; kb += step) {
@@ -564,7 +579,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
-            const int mb = w.t / p.n_tiles, nb = w.t - mb * p.n_tiles;
+            int mb, nb;
+            tile_coords(w.t, p, mb, nb);
             // 128-column block of the output this warp's columns fall in
             const int jb = (nb * BN + half * COLS) >> 7;
             const bool jvalid = jb < p.nb_valid;
