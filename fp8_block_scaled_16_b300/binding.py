@@ -56,6 +56,8 @@ SIGNATURES = {
     "fp8bs_gemm_workspace_bytes": (_I64, [ctypes.c_int, _I64, _I64, _I64]),
     "fp8bs_gemm_group": (ctypes.c_int, [ctypes.POINTER(GemmArgs), ctypes.c_int, _P]),
     "fp8bs_debug_split_plan": (ctypes.c_int, [_I64, _I64, ctypes.c_int, _P]),
+    "fp8bs_debug_tile_order": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int32, _I64, _I64, _I64, ctypes.c_int32,
+                                              _P]),
     "fp8bs_gemm_wgrad_workspace_bytes": (_I64, [_I64, _I64, _I64]),
     "fp8bs_gemm_wgrad_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8bs_gemm_wgrad_accumulate_f32": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -398,6 +400,17 @@ def fp8bs_debug_split_plan(tiles: int, kblocks: int, sms: int) -> dict:
     _check(load().fp8bs_debug_split_plan(tiles, kblocks, sms, ctypes.cast(out, ctypes.c_void_p)),
            "fp8bs_debug_split_plan")
     return {"splits": out[0], "tail_first": out[1], "units": out[2], "bytes": out[3]}
+
+
+def fp8bs_debug_tile_order(m_tiles: int, n_tiles: int, kc: int, splits: int = 1, tail_first: int = 0,
+                           grid: int = 148, l2_bytes: int = 126 << 20, out_bytes: int = 2) -> dict:
+    """The tile order a GEMM launch would take (host computation only):
+    column-strip width (== n_tiles: row-major) and the estimated DRAM bytes
+    of operand panels for that order and for row-major."""
+    out = (ctypes.c_int64 * 3)()
+    _check(load().fp8bs_debug_tile_order(m_tiles, n_tiles, kc, splits, tail_first, grid, l2_bytes, out_bytes,
+                                         ctypes.cast(out, ctypes.c_void_p)), "fp8bs_debug_tile_order")
+    return {"strip": out[0], "dram_bytes": out[1], "row_major_dram_bytes": out[2]}
 
 
 def fp8bs_gemm_group(members, stream=None, split=True):

@@ -79,6 +79,19 @@ WORKLOADS: Dict[str, Workload] = {
                     "(unit variance); W ~N(0,0.02); dY ~N(0,1e-3); fprop + dgrad + wgrad"),
 }
 
+# The decoder layer at fewer tokens (same recipe and seed): small cases for
+# profiler captures whose DRAM traffic is scaled to 32768 tokens.
+for _tokens in (8192, 16384):
+    _name = f"decoder_layer_{_tokens}"
+    WORKLOADS[_name] = dataclasses.replace(
+        WORKLOADS["decoder_layer_32768"], name=_name,
+        linears=tuple(dataclasses.replace(lin, tokens=_tokens) for lin in WORKLOADS["decoder_layer_32768"].linears),
+        description=f"the decoder layer's four linears at {_tokens} tokens (profiling cases)")
+
+# The five configurations of the benchmark's metric, in order.
+CONFIGS = ("tiny_fprop_256x512x512", "attn_qkv_fprop_8192x3072x2048", "mlp_gate_up_16384x11264x2048",
+           "mlp_down_16384x2048x5632", "decoder_layer_32768")
+
 WEIGHT_STD = 0.02
 GRAD_STD = 1e-3
 

@@ -367,6 +367,17 @@ int64_t fp8bs_debug_tensor_map_encodes(void);
  *     device needed): out[0] splits (1 = none), out[1] the first split tile
  *     (tiles before it are whole), out[2] work units, out[3] scratch bytes.
  *     FP8BS_ERR_INVALID_ARG for non-positive sizes or a NULL `out`.
+ *   fp8bs_debug_tile_order: the tile order a GEMM launch would use, host
+ *     only: the output's m_tiles x n_tiles tiles (128 x 256), contraction of
+ *     kc bytes per operand row, split plan (`splits`, `tail_first` as
+ *     fp8bs_debug_split_plan gives them), `grid` persistent CTAs, an L2 of
+ *     `l2_bytes` and `out_bytes` (1, 2 or 4) per output element.  The GEMMs
+ *     take tiles in column strips out[0] tiles wide (row-major inside a
+ *     strip; out[0] == n_tiles is plain row-major), the width with the
+ *     fewest DRAM bytes of operand panels by a wave-by-wave L2 reuse
+ *     estimate: out[1] those bytes for the chosen order, out[2] for
+ *     row-major.  FP8BS_ERR_INVALID_ARG for non-positive sizes, more than
+ *     2^30 tiles, a bad split or `out_bytes`, or a NULL `out`.
  */
 int fp8bs_debug_set_wait_timeout_ns(int64_t ns);
 #define FP8BS_DEBUG_F32_OUT 1u
@@ -375,6 +386,8 @@ int fp8bs_debug_occupy_sms(int ctas, int64_t ns, void* stream);
 int fp8bs_debug_set_fault(int mode);
 int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
 int fp8bs_debug_split_plan(int64_t tiles, int64_t kblocks, int sms, int64_t* out);
+int fp8bs_debug_tile_order(int64_t m_tiles, int64_t n_tiles, int64_t kc, int32_t splits, int64_t tail_first,
+                           int64_t grid, int64_t l2_bytes, int32_t out_bytes, int64_t* out);
 int fp8bs_debug_silu_mul(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h, void* stream);
 
 #ifdef __cplusplus
