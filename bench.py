@@ -476,10 +476,13 @@ def padded(m):
     return (m + 127) // 128 * 128
 
 
-def sample_note(feats, rows, tokens=128):
-    return (f"each linear restricted to its first {tokens} tokens and first {feats} output features (all input "
-            f"features): X and dY quantized both ways, W[:{feats}] quantized 128x128, {rows} output rows of "
-            f"fprop, dgrad and wgrad; single-threaded C oracle")
+def sample_note(feats, rows, tokens=128, max_features=11264):
+    if feats >= max_features:
+        which, wpart = "all output and input features", "W"
+    else:
+        which, wpart = f"its first {feats} output features (all input features)", f"W[:{feats}]"
+    return (f"each linear restricted to its first {tokens} tokens and {which}: X and dY quantized both ways, "
+            f"{wpart} quantized 128x128, {rows} output rows of fprop, dgrad and wgrad; single-threaded C oracle")
 
 
 KERNEL_OF_OP = {
@@ -674,7 +677,8 @@ def run_ours(args):
         fl, sec = cpu_sample(list(zip(wl.linears, data)), args.cpu_feats, args.cpu_rows)
         result["cpu_baseline"] = {
             "value": fl / sec / 1e12, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
-            "sample": sample_note(args.cpu_feats, args.cpu_rows) + f", {sec:.1f} s"}
+            "sample": sample_note(args.cpu_feats, args.cpu_rows,
+                                  max_features=max(lin.out_features for lin in wl.linears)) + f", {sec:.1f} s"}
         if not args.no_cpu_configs:
             per_cfg, sec_cfg = cpu_per_config()
             result["cpu_baseline"]["per_config"] = per_cfg
@@ -742,7 +746,7 @@ def run_reference(args):
         fl += f
         sec += s
     value = fl / sec / 1e12
-    note = sample_note(feats, rows)
+    note = sample_note(feats, rows, max_features=max(lin.out_features for lin in wl.linears))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
