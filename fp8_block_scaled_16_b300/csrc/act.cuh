@@ -22,41 +22,61 @@
 
 namespace fp8bs {
 
-__device__ __forceinline__ float exp_cw(float x) {
-    if (x > 88.0f) return __int_as_float(0x7f800000);
-    if (x < -87.0f) return 0.0f;
-    const float n = rintf(__fmul_rn(x, 1.44269502f));             // log2(e) in FP32
-    float r = __fmaf_rn(-n, 0.693145751953125f, x);               // ln 2, high part: 45426 / 2^16
-    r = __fmaf_rn(-n, 1.42860677e-06f, r);                        // ln 2 - high part
-    float p = 1.0f / 5040.0f;
-    p = __fmaf_rn(p, r, 1.0f / 720.0f);
-    p = __fmaf_rn(p, r, 1.0f / 120.0f);
-    p = __fmaf_rn(p, r, 1.0f / 24.0f);
-    p = __fmaf_rn(p, r, 1.0f / 6.0f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
+// e^x of two values with packed FP32 operations; each lane of a packed
+// multiply or fused multiply-add rounds like the scalar operation, so every
+// lane follows the scalar steps: n = rint(x log2 e) (log2 e rounded to
+// FP32), r = x - n ln2 in two fused steps (ln 2's high part 45426 / 2^16,
+// then the rest), the degree-7 Taylor polynomial of e^r in Horner form, and
+// the product with 2^n.  Lanes above 88 give +Inf, below -87 give 0; they
+// are evaluated on the clamped value, whose result is then replaced.
+__device__ __forceinline__ float2 exp_cw2(float2 x) {
+    const float2 xc = make_float2(fminf(fmaxf(x.x, -87.0f), 88.0f), fminf(fmaxf(x.y, -87.0f), 88.0f));
+    const float2 m = __fmul2_rn(xc, make_float2(1.44269502f, 1.44269502f));
+    const float2 n = make_float2(rintf(m.x), rintf(m.y));
+    const float2 nn = make_float2(-n.x, -n.y);
+    float2 r = __ffma2_rn(nn, make_float2(0.693145751953125f, 0.693145751953125f), xc);
+    r = __ffma2_rn(nn, make_float2(1.42860677e-06f, 1.42860677e-06f), r);
+    float2 p = make_float2(1.0f / 5040.0f, 1.0f / 5040.0f);
+    p = __ffma2_rn(p, r, make_float2(1.0f / 720.0f, 1.0f / 720.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f / 120.0f, 1.0f / 120.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f / 24.0f, 1.0f / 24.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+    p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    const float2 two_n = make_float2(__int_as_float((static_cast<int>(n.x) + 127) << 23),
+                                     __int_as_float((static_cast<int>(n.y) + 127) << 23));
+    float2 e = __fmul2_rn(p, two_n);
+    const float inf = __int_as_float(0x7f800000);
+    if (x.x > 88.0f) e.x = inf;
+    if (x.x < -87.0f) e.x = 0.0f;
+    if (x.y > 88.0f) e.y = inf;
+    if (x.y < -87.0f) e.y = 0.0f;
+    return e;
 }
 
-// FP32 h = SiLU(g) * u for BF16-valued g and u (before the final rounding).
-__device__ __forceinline__ float silu_mul_f32(float g, float u) {
-    const float d = __fadd_rn(1.0f, exp_cw(-g));
-    return __fmul_rn(__fdiv_rn(g, d), u);
+// FP32 h = SiLU(g) * u = g / (1 + e^-g) * u for two pairs of BF16-valued g
+// and u (before the final rounding): one IEEE rounding per operation.
+__device__ __forceinline__ float2 silu_mul2_f32(float2 g, float2 u) {
+    const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), exp_cw2(make_float2(-g.x, -g.y)));
+    return __fmul2_rn(make_float2(__fdiv_rn(g.x, d.x), __fdiv_rn(g.y, d.y)), u);
 }
 
-// The same as a called function: the GEMM epilogue evaluates it for 128
-// values per thread, and 128 inlined copies would crowd the instruction
-// cache that the K-block loop runs from.
-__device__ __noinline__ float silu_mul_call(float g, float u) { return silu_mul_f32(g, u); }
-
-// Test kernel: h[i] = bf16(SiLU(g[i]) * u[i]) on BF16 bit patterns.
+// Test kernel: h[i] = bf16(SiLU(g[i]) * u[i]) on BF16 bit patterns, two
+// elements per evaluation as in the GEMM epilogue (an odd last element is
+// paired with itself).
 __global__ void silu_mul_kernel(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* h) {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+    const int64_t pairs = (n + 1) / 2;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < pairs;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const float v = silu_mul_f32(__uint_as_float(static_cast<uint32_t>(g[i]) << 16),
-                                     __uint_as_float(static_cast<uint32_t>(u[i]) << 16));
-        h[i] = static_cast<uint16_t>(f32x2_to_bf16x2(v, 0.0f) & 0xFFFFu);
+        const int64_t a = 2 * i, b = a + 1 < n ? a + 1 : a;
+        const float2 v = silu_mul2_f32(make_float2(__uint_as_float(static_cast<uint32_t>(g[a]) << 16),
+                                                   __uint_as_float(static_cast<uint32_t>(g[b]) << 16)),
+                                       make_float2(__uint_as_float(static_cast<uint32_t>(u[a]) << 16),
+                                                   __uint_as_float(static_cast<uint32_t>(u[b]) << 16)));
+        const uint32_t w = f32x2_to_bf16x2(v.x, v.y);
+        h[a] = static_cast<uint16_t>(w & 0xFFFFu);
+        if (b != a) h[b] = static_cast<uint16_t>(w >> 16);
     }
 }
 

@@ -119,9 +119,12 @@ struct Tile {
     static constexpr int OUT_BOX_BYTES = 32 * 64 * 2;
     static constexpr int OFF_OUT = (OFF_SCALE + SSLOTS * SLOT_FLOATS * 4 + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_OUT + NUM_EPI_WARPS * 2 * OUT_BOX_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + NBUF + 2 * SSLOTS + 8;
+    static constexpr int NUM_BARS = 2 * STAGES + NBUF + 2 * SSLOTS + 12;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+    // SwiGLU epilogue: per quadrant and column half, the 32 rows' partial amax
+    // of H as BF16 bits (H is BF16, so its amax is too).
+    static constexpr int OFF_AMAX = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = OFF_AMAX + 4 * 2 * 32 * 2 + 1024;  // + slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment for 128-byte swizzle");
     static_assert(COLS == 128, "epilogue chunking assumes 128 columns per warp");
@@ -136,9 +139,12 @@ struct Tile {
     static __device__ __forceinline__ uint32_t tempty(int b) { return 2 * STAGES + b; }
     static __device__ __forceinline__ uint32_t sfull(int i) { return 2 * STAGES + NBUF + i; }
     static __device__ __forceinline__ uint32_t sempty(int i) { return 2 * STAGES + NBUF + SSLOTS + i; }
-    // SwiGLU epilogue: the up half of quadrant q's rows handed to the gate half.
-    static __device__ __forceinline__ uint32_t xfull(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + q; }
-    static __device__ __forceinline__ uint32_t xempty(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + 4 + q; }
+    // SwiGLU epilogue, per quadrant q (the gate and the up warp of its rows):
+    // xhalf -- both have staged the half the other needs; xamax -- both have
+    // published their partial amax; xq8 -- the up warp's FP8 half is staged.
+    static __device__ __forceinline__ uint32_t xhalf(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + q; }
+    static __device__ __forceinline__ uint32_t xamax(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + 4 + q; }
+    static __device__ __forceinline__ uint32_t xq8(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + 8 + q; }
 };
 
 struct Params {
@@ -367,6 +373,73 @@ __device__ __forceinline__ void promote_rank1(float (&acc)[N], int base_lo, int 
     }
 }
 
+// SwiGLU epilogue helpers (one 64-column half of a warp's 128 accumulator
+// columns, offsets fixed at compile time so that acc stays in registers).
+// A staging box row is 128 bytes: 16-byte chunk c of row r at c ^ (r % 8).
+template <int J0, int N>
+__device__ __forceinline__ void stage_bf16_64(const float (&acc)[N], uint32_t box, int lane) {
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+        const int j = J0 + c * 8;
+        const uint32_t a = box + static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(f32x2_to_bf16x2(acc[j], acc[j + 1])),
+                     "r"(f32x2_to_bf16x2(acc[j + 2], acc[j + 3])), "r"(f32x2_to_bf16x2(acc[j + 4], acc[j + 5])),
+                     "r"(f32x2_to_bf16x2(acc[j + 6], acc[j + 7]))
+                     : "memory");
+    }
+}
+
+// H = bf16(SiLU(G) * U) for acc[J0 .. J0+63] (this warp's gate values if
+// GATE, else its up values) with the other operand's BF16 half from `peer`;
+// the BF16 H values replace acc and their amax is returned.
+template <int J0, bool GATE, int N>
+__device__ __forceinline__ float swiglu_64(float (&acc)[N], uint32_t peer, int lane) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+        const int j = J0 + c * 8;
+        uint32_t pw[4];
+        const uint32_t a = peer + static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(pw[0]), "=r"(pw[1]), "=r"(pw[2]), "=r"(pw[3])
+                     : "r"(a)
+                     : "memory");
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const uint32_t ow = f32x2_to_bf16x2(acc[j + 2 * e], acc[j + 2 * e + 1]);
+            const uint32_t gw = GATE ? ow : pw[e];
+            const uint32_t uw = GATE ? pw[e] : ow;
+            const float2 h = silu_mul2_f32(make_float2(bf16lo_to_f32(gw), bf16hi_to_f32(gw)),
+                                           make_float2(bf16lo_to_f32(uw), bf16hi_to_f32(uw)));
+            const uint32_t hw = f32x2_to_bf16x2(h.x, h.y);
+            acc[j + 2 * e] = bf16lo_to_f32(hw);
+            acc[j + 2 * e + 1] = bf16hi_to_f32(hw);
+            amax = fmaxf(amax, fmaxf(fabsf(acc[j + 2 * e]), fabsf(acc[j + 2 * e + 1])));
+        }
+    }
+    return amax;
+}
+
+// E4M3 codes of acc[J0 .. J0+63] * inv into 16-byte chunks CH0 .. CH0+3 of a
+// 128-byte FP8 row.
+template <int J0, int CH0, int N>
+__device__ __forceinline__ void stage_fp8_64(const float (&acc)[N], float inv, uint32_t box, int lane) {
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int j = J0 + c * 16 + q * 4;
+            wv[q] = e4m3x2(__fmul_rn(acc[j], inv), __fmul_rn(acc[j + 1], inv)) |
+                    (e4m3x2(__fmul_rn(acc[j + 2], inv), __fmul_rn(acc[j + 3], inv)) << 16);
+        }
+        const uint32_t a = box + static_cast<uint32_t>(lane * 128 + (((CH0 + c) ^ (lane & 7)) << 4));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]), "r"(wv[2]),
+                     "r"(wv[3])
+                     : "memory");
+    }
+}
+
 template <int SBMODE, int BN, int G, int EPI>
 __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ Group<G> grp) {
     static_assert(EPI == EPI_PLAIN || (SBMODE == SB_SCALAR && G == 1), "FP8 epilogues: single forward products");
@@ -388,8 +461,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         }
         for (int b = 0; b < NBUF; b++) mbar_init(bar(T::tempty(b)), NUM_EPI_WARPS);
         for (int q = 0; q < 4; q++) {
-            mbar_init(bar(T::xfull(q)), 1);
-            mbar_init(bar(T::xempty(q)), 1);
+            mbar_init(bar(T::xhalf(q)), 2);
+            mbar_init(bar(T::xamax(q)), 2);
+            mbar_init(bar(T::xq8(q)), 1);
         }
         for (int i = 0; i < SSLOTS; i++) {
             mbar_init(bar(T::sfull(i)), 32);   // one cp.async arrival per lane of the scale warp
@@ -575,7 +649,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         const int row = quad * 32 + lane;
         const float* ring = reinterpret_cast<const float*>(smem + T::OFF_SCALE);
         int tb = 0, slot = 0, stage = 0;
-        uint32_t sph = 0, xph = 0, ph = 0;
+        uint32_t sph = 0, xph = 0, q8ph = 0, ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
@@ -715,106 +789,71 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             }
             if constexpr (SBMODE == SB_SCALAR) {
                 if constexpr (EPI == EPI_SWIGLU) {
-                    // SwiGLU: half 0 holds the gate values of this 128-wide H block,
-                    // half 1 the up values of the same rows and columns.  The up warp
-                    // hands its BF16 row to the gate warp of its quadrant through its
-                    // (otherwise unused) staging buffer: 32 rows x 256 bytes, 16-byte
-                    // chunk c of row r at c ^ (r % 16).
-                    const uint32_t xbuf = sbase + T::OFF_OUT + static_cast<uint32_t>((quad + 4) * 2 * T::OUT_BOX_BYTES);
-                    if (half == 1) {
-                        if (!warp_wait_bounded(bar(T::xempty(quad)), xph ^ 1u, wc)) { ok = false; break; }
-#pragma unroll
-                        for (int c = 0; c < 16; c++) {
-                            const int j = c * 8;
-                            const uint32_t a = xbuf + static_cast<uint32_t>(lane * 256 + ((c ^ (lane & 15)) << 4));
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                         "r"(f32x2_to_bf16x2(acc[j], acc[j + 1])), "r"(f32x2_to_bf16x2(acc[j + 2], acc[j + 3])),
-                                         "r"(f32x2_to_bf16x2(acc[j + 4], acc[j + 5])), "r"(f32x2_to_bf16x2(acc[j + 6], acc[j + 7]))
-                                         : "memory");
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(T::xfull(quad)));
-                        xph ^= 1u;
-                        continue;
-                    }
-                    if (!warp_wait_bounded(bar(T::xfull(quad)), xph, wc)) { ok = false; break; }
-                    float amax = 0.0f;
-#pragma unroll
-                    for (int c = 0; c < 16; c++) {
-                        const int j = c * 8;
-                        uint32_t uw[4];
-                        const uint32_t a = xbuf + static_cast<uint32_t>(lane * 256 + ((c ^ (lane & 15)) << 4));
-                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(uw[0]), "=r"(uw[1]), "=r"(uw[2]), "=r"(uw[3])
-                                     : "r"(a)
-                                     : "memory");
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            const uint32_t gw = f32x2_to_bf16x2(acc[j + 2 * e], acc[j + 2 * e + 1]);
-                            const float h0 = silu_mul_call(bf16lo_to_f32(gw), bf16lo_to_f32(uw[e]));
-                            const float h1 = silu_mul_call(bf16hi_to_f32(gw), bf16hi_to_f32(uw[e]));
-                            const uint32_t hw = f32x2_to_bf16x2(h0, h1);
-                            acc[j + 2 * e] = bf16lo_to_f32(hw);
-                            acc[j + 2 * e + 1] = bf16hi_to_f32(hw);
-                            amax = fmaxf(amax, fmaxf(fabsf(acc[j + 2 * e]), fabsf(acc[j + 2 * e + 1])));
-                        }
-                    }
+                    // SwiGLU: half 0 holds the gate values G of this 128-wide H block,
+                    // half 1 the up values U of the same rows and columns.  The two
+                    // warps of a quadrant share the activation: each hands the other,
+                    // in the first box of its staging buffer (32 rows x 128 bytes,
+                    // 16-byte chunk c of row r at c ^ (r % 8)), the BF16 half it needs
+                    // -- the gate warp G[64..127], the up warp U[0..63] -- then the
+                    // gate warp computes H[0..63] and the up warp H[64..127] and each
+                    // stores its BF16 half.  The row's amax is combined through
+                    // shared memory, and both FP8 halves are staged in the gate
+                    // warp's first box for one TMA store.
+                    const uint32_t own0 = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
+                    const uint32_t own1 = own0 + static_cast<uint32_t>(T::OUT_BOX_BYTES);
+                    const uint32_t peer0 = sbase + T::OFF_OUT + static_cast<uint32_t>((ew ^ 4) * 2 * T::OUT_BOX_BYTES);
+                    const uint32_t gate0 = sbase + T::OFF_OUT + static_cast<uint32_t>(quad * 2 * T::OUT_BOX_BYTES);
+                    const int mine = half * 64;  // H columns this warp computes
+                    // This warp's TMA stores of the previous tile have read its boxes.
+                    if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(T::xempty(quad)));
-                    xph ^= 1u;
-                    // H block nb: BF16 (optional), then its 1x128 quantization.
+                    if (half == 0) stage_bf16_64<64>(acc, own0, lane);
+                    else stage_bf16_64<0>(acc, own0, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::xhalf(quad)));
+                    if (!warp_wait_bounded(bar(T::xhalf(quad)), xph, wc)) { ok = false; break; }
+                    float amax = half == 0 ? swiglu_64<0, true>(acc, peer0, lane) : swiglu_64<64, false>(acc, peer0, lane);
+                    // Partial amax (a BF16 value) to the partner; both then hold the row's amax.
+                    uint16_t* amx = reinterpret_cast<uint16_t*>(smem + T::OFF_AMAX);
+                    amx[(quad * 2 + half) * 32 + lane] = static_cast<uint16_t>(__float_as_uint(amax) >> 16);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::xamax(quad)));
                     const bool hvalid = static_cast<int64_t>(mb) * BM + quad * 32 < p.rows;
-                    const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
                     if (hvalid && p.out_bf16) {
-                        if (lane == 0) bulk_wait_read_all();
-                        __syncwarp();
-#pragma unroll
-                        for (int b = 0; b < 2; b++) {
-#pragma unroll
-                            for (int c = 0; c < 8; c++) {
-                                const int j = b * 64 + c * 8;
-                                const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
-                                                                                     ((c ^ (lane & 7)) << 4));
-                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                             "r"(f32x2_to_bf16x2(acc[j], acc[j + 1])), "r"(f32x2_to_bf16x2(acc[j + 2], acc[j + 3])),
-                                             "r"(f32x2_to_bf16x2(acc[j + 4], acc[j + 5])), "r"(f32x2_to_bf16x2(acc[j + 6], acc[j + 7]))
-                                             : "memory");
-                            }
-                        }
+                        // This warp's 64 columns of H in BF16.
+                        if (half == 0) stage_bf16_64<0>(acc, own1, lane);
+                        else stage_bf16_64<64>(acc, own1, lane);
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&grp.tmC[g], stage_out, nb * COLS, mb * BM + quad * 32);
-                            tma_store_2d(&grp.tmC[g], stage_out + T::OUT_BOX_BYTES, nb * COLS + 64, mb * BM + quad * 32);
+                            tma_store_2d(&grp.tmC[g], own1, nb * COLS + mine, mb * BM + quad * 32);
                             bulk_commit_group();
                         }
                     }
+                    if (!warp_wait_bounded(bar(T::xamax(quad)), xph, wc)) { ok = false; break; }
+                    xph ^= 1u;
+                    amax = fmaxf(amax, __uint_as_float(static_cast<uint32_t>(amx[(quad * 2 + (half ^ 1)) * 32 + lane]) << 16));
                     float sq, inv;
                     tile_scale(amax, sq, inv);
-                    p.out_s[static_cast<int64_t>(nb) * p.sa_ld + static_cast<int64_t>(mb) * BM + row] = sq;
+                    if (half == 0) p.out_s[static_cast<int64_t>(nb) * p.sa_ld + static_cast<int64_t>(mb) * BM + row] = sq;
                     if (hvalid) {
-                        if (lane == 0) bulk_wait_read_all();
-                        __syncwarp();
-#pragma unroll
-                        for (int c = 0; c < 8; c++) {
-                            uint32_t wv[4];
-#pragma unroll
-                            for (int q = 0; q < 4; q++) {
-                                const int j = c * 16 + q * 4;
-                                wv[q] = e4m3x2(__fmul_rn(acc[j], inv), __fmul_rn(acc[j + 1], inv)) |
-                                        (e4m3x2(__fmul_rn(acc[j + 2], inv), __fmul_rn(acc[j + 3], inv)) << 16);
-                            }
-                            const uint32_t a = stage_out + static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4));
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]),
-                                         "r"(wv[2]), "r"(wv[3])
-                                         : "memory");
-                        }
+                        // Both warps have read their handed-over halves (they published
+                        // their amax after that), so the gate warp's first box is free
+                        // for the FP8 row: chunks 0-3 from the gate warp, 4-7 from the up warp.
+                        if (half == 0) stage_fp8_64<0, 0>(acc, inv, gate0, lane);
+                        else stage_fp8_64<64, 4>(acc, inv, gate0, lane);
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&grp.tmQ[g], stage_out, nb * COLS, mb * BM + quad * 32);
-                            bulk_commit_group();
+                        if (half == 1) {
+                            if (lane == 0) mbar_arrive(bar(T::xq8(quad)));
+                        } else {
+                            if (!warp_wait_bounded(bar(T::xq8(quad)), q8ph, wc)) { ok = false; break; }
+                            if (lane == 0) {
+                                tma_store_2d(&grp.tmQ[g], gate0, nb * COLS, mb * BM + quad * 32);
+                                bulk_commit_group();
+                            }
                         }
+                        q8ph ^= 1u;
                     }
                     continue;
                 }
