@@ -66,6 +66,7 @@ SIGNATURES = {
     "fp8bs_debug_tensor_map_encodes": (_I64, []),
     "fp8bs_debug_set_wait_timeout_ns": (ctypes.c_int, [_I64]),
     "fp8bs_debug_set_fault": (ctypes.c_int, [ctypes.c_int]),
+    "fp8bs_debug_force_tile_order": (ctypes.c_int, [ctypes.c_int]),
     "fp8bs_debug_set_flags": (ctypes.c_int, [ctypes.c_uint]),
     "fp8bs_debug_occupy_sms": (ctypes.c_int, [ctypes.c_int, _I64, _P]),
     "fp8bs_debug_e4m3_encode_bits": (ctypes.c_int, [ctypes.c_uint32, _I64, _P, _P]),
@@ -380,6 +381,12 @@ def fp8bs_debug_set_flags(flags: int) -> None:
     global _debug_flags
     _check(load().fp8bs_debug_set_flags(flags), "fp8bs_debug_set_flags")
     _debug_flags = flags
+
+
+def fp8bs_debug_force_tile_order(strip: int) -> None:
+    """Test hook: GEMMs take tiles in column strips `strip` wide (0: the
+    library's own choice per shape)."""
+    _check(load().fp8bs_debug_force_tile_order(strip), "fp8bs_debug_force_tile_order")
 
 
 def fp8bs_debug_set_fault(mode: int) -> None:

@@ -48,6 +48,7 @@ constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 std::atomic<int64_t> g_launches{0};
 std::atomic<int64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_fault{0};
+std::atomic<int> g_force_strip{0};  // test hook: tile-order strip width (0: chosen per shape)
 std::atomic<unsigned> g_debug_flags{0};
 
 struct DeviceInfo {
@@ -405,6 +406,11 @@ int32_t choose_strip(int64_t m_tiles, int64_t n_tiles, int64_t kc, int32_t split
 
 // Sets member p's tile order for the work units it will run (after its split plan).
 void set_raster(const DeviceInfo* d, gemm::Params* p, int64_t units) {
+    const int forced = g_force_strip.load();
+    if (forced > 0) {
+        p->strip = std::min<int32_t>(forced, p->n_tiles);
+        return;
+    }
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(units, d->sm_count));
     const int32_t out_bytes = p->out_f32_add != 0 ? 4 : (p->out_bf16 ? 2 : 1);
     p->strip = choose_strip(p->m_tiles, p->n_tiles, static_cast<int64_t>(p->kblocks) * gemm::BK, p->splits,
@@ -866,6 +872,12 @@ int fp8bs_debug_occupy_sms(int ctas, int64_t ns, void* stream) {
 int fp8bs_debug_set_flags(unsigned flags) {
     if (flags & ~static_cast<unsigned>(FP8BS_DEBUG_F32_OUT)) return FP8BS_ERR_INVALID_ARG;
     g_debug_flags.store(flags);
+    return FP8BS_OK;
+}
+
+int fp8bs_debug_force_tile_order(int strip) {
+    if (strip < 0) return FP8BS_ERR_INVALID_ARG;
+    fp8bs::g_force_strip.store(strip);
     return FP8BS_OK;
 }
 

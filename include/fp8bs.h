@@ -342,6 +342,12 @@ int64_t fp8bs_debug_tensor_map_encodes(void);
  * Test hooks (not for production use).
  *   fp8bs_debug_set_wait_timeout_ns: the limit of every bounded device wait
  *     (default 2e9 ns); 0 restores the default.
+ *   fp8bs_debug_force_tile_order: GEMM launches take their tiles in column
+ *     strips `strip` tiles wide (capped at the output's tile columns; 1:
+ *     column by column) instead of the order fp8bs_debug_tile_order would
+ *     choose, until reset with 0.  Outputs do not depend on the order except
+ *     through which tiles a split plan splits (the split tiles are the last
+ *     ones in that order).  FP8BS_ERR_INVALID_ARG for a negative width.
  *   fp8bs_debug_set_fault: when 1, the next GEMM launch withholds one
  *     operand copy so that the kernel's bounded wait expires and it reports
  *     FP8BS_ERR_TIMEOUT without faulting; reset to 0 after that launch.
@@ -383,6 +389,7 @@ int fp8bs_debug_set_wait_timeout_ns(int64_t ns);
 #define FP8BS_DEBUG_F32_OUT 1u
 int fp8bs_debug_set_flags(unsigned flags);
 int fp8bs_debug_occupy_sms(int ctas, int64_t ns, void* stream);
+int fp8bs_debug_force_tile_order(int strip);
 int fp8bs_debug_set_fault(int mode);
 int fp8bs_debug_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
 int fp8bs_debug_split_plan(int64_t tiles, int64_t kblocks, int sms, int64_t* out);

@@ -228,6 +228,49 @@ def test_forward_and_data_gradient_tail_split(op):
     assert_gemm_close(np_bf16_bits(unsplit)[rows], acc, sab, f"unsplit {op}")
 
 
+def test_tile_order_does_not_change_outputs():
+    """The persistent CTAs' tile order (column strips of any width, the last
+    one ragged, row-major, column by column) moves only which CTA computes
+    a tile: unsplit products are bitwise equal in every order.  A product
+    whose split plan splits every tile (uniform parts) is too, since no
+    order changes which tiles are split."""
+    M, N, K = 1000, 1792, 768   # 8 x 7 forward tiles, 8 x 3 data-gradient, 14 x 3 weight-gradient
+    x = inputs.random_bf16((M, K), seed=311)
+    x[:, 7] *= 25.0
+    w = inputs.random_bf16((N, K), seed=312, std=0.02)
+    dy = inputs.random_bf16((M, N), seed=313, std=1e-3)
+    xq, sx, xTq, sxT = B.fp8bs_quantize_act(x.cuda(), B.ROWWISE | B.COLWISE_T)
+    wq, wqT, sw = B.fp8bs_quantize_weight(w.cuda(), want_t=True)
+    dyq, sdy, dyTq, sdyT = B.fp8bs_quantize_act(dy.cuda(), B.ROWWISE | B.COLWISE_T)
+    Ms, Ns, Ks = 8192, 256, 512  # weight gradient of 2 x 2 tiles over 64 K blocks
+    xs = inputs.random_bf16((Ms, Ks), seed=314)
+    dys = inputs.random_bf16((Ms, Ns), seed=315, std=1e-3)
+    _, _, xsTq, sxsT = B.fp8bs_quantize_act(xs.cuda(), B.COLWISE_T)
+    _, _, dysTq, sdysT = B.fp8bs_quantize_act(dys.cuda(), B.COLWISE_T)
+    plan = B.fp8bs_debug_split_plan(4, Ms // 128, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["splits"] > 1 and plan["tail_first"] == 0, plan
+
+    def run():
+        outs = [B.fp8bs_gemm_fprop(xq, sx, wq, sw, split=False), B.fp8bs_gemm_dgrad(dyq, sdy, wqT, sw, split=False),
+                B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT, split=False), B.fp8bs_gemm_wgrad(dysTq, sdysT, xsTq, sxsT)]
+        assert B.fp8bs_get_device_status() == 0
+        return [o.view(torch.int16).clone() for o in outs]
+
+    ref = run()
+    try:
+        for strip in (1, 2, 3, 5, 64):
+            B.fp8bs_debug_force_tile_order(strip)
+            got = run()
+            for name, a, b in zip(("fprop", "dgrad", "wgrad", "split wgrad"), got, ref):
+                assert torch.equal(a, b), f"{name} differs with strips of {strip}"
+    finally:
+        B.fp8bs_debug_force_tile_order(0)
+    oxq, osx = oracle.quant_rowwise_1x128(x)
+    owq, _, osw = oracle.quant_weight_128x128(w, want_t=False)
+    acc, _, sab = oracle_gemm_rows("fprop", oxq, osx, owq, osw, np.arange(M))
+    assert_gemm_close(np_bf16_bits(ref[0].view(torch.bfloat16)), acc, sab, "fprop")
+
+
 def test_grouped_launch_equals_single_launches():
     """Products of different shapes (a token tail, ragged output tiles) in
     one launch: forward and data-gradient products together, weight
