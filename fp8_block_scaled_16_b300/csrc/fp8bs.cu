@@ -1,6 +1,7 @@
 // fp8bs.cu -- host side of the C ABI declared in include/fp8bs.h: argument
-// validation, TMA tensor-map encoding, kernel launches on the caller's
-// stream, and the per-device status word.
+// validation, TMA tensor-map encoding (cached), split-K and tile-order
+// planning for the GEMMs, kernel launches on the caller's stream, and the
+// per-device status word.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

@@ -36,7 +36,9 @@
 //       result through swizzled shared staging and TMA: BF16 stores, FP32
 //       reduce-adds for an accumulating weight gradient, and/or, for a
 //       forward product, the output's 1x128 E4M3 quantization (a thread's
-//       128 columns are one whole tile).
+//       128 columns are one whole tile); for a gate+up product, H =
+//       SiLU(G) * U and its 1x128 quantization, the gate and the up warp of
+//       a row each computing half of H.
 // While the epilogue promotes block b, the tensor cores already compute
 // block b+1 into the other buffer.
 //
@@ -44,7 +46,10 @@
 // of tiles would leave many SMs idle, 2-8 splits of the contraction of some
 // or all tiles, whose FP32 partials meet in caller-provided scratch (see
 // Params::splits).  One launch may compute several products (Group): their
-// units are dealt to the persistent CTAs as one list.  Rows past the
+// units are dealt to the persistent CTAs as one list.  Tiles are taken in
+// column strips Params::strip tiles wide (row-major when strip == n_tiles),
+// a width the host picks per shape to limit DRAM re-reads of operand
+// panels; only which tiles a split plan splits depends on it.  Rows past the
 // output's last row (a token count that is not a multiple of 128) read zeros
 // through TMA and are not stored.
 //
@@ -150,8 +155,8 @@ struct Tile {
 struct Params {
     int32_t m_tiles, n_tiles, kblocks;
     // Tile order: column strips `strip` tiles wide, row-major inside a strip
-    // (strip == n_tiles: plain row-major), chosen by the host so that the
-    // tiles running at once touch few distinct A and B panels.
+    // (strip == n_tiles: plain row-major), chosen by the host for the fewest
+    // estimated DRAM re-reads of A and B panels across waves of tiles.
     int32_t strip;
     int32_t nb_valid;             // number of 128-column blocks of the output (cols / 128)
     int64_t rows, cols;           // output shape (rows need not be a multiple of 128)
