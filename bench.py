@@ -634,7 +634,7 @@ def run_ours(args):
     breakdown = {}
     for k, s in sorted(agg.items(), key=lambda kv: -kv[1]["ms"]):
         if s["unit"] == "flops":
-            r, u, pk = s["work"] / (s["ms"] * 1e-3) / 1e12, "TFLOP/s", fp8_burst
+            r, u, pk = s["work"] / (s["ms"] * 1e-3) / 1e12, "TFLOP/s", fp8_sust if long_region else fp8_burst
         else:
             r, u, pk = s["work"] / (s["ms"] * 1e-3) / 1e9, "GB/s", peaks["hbm_gbs"]
         breakdown[k] = {"ops": sorted(s["ops"]), "launches_per_step": s["launches"] // args.steps,
