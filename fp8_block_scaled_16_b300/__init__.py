@@ -2,7 +2,8 @@
 
 The compute lives in the CUDA library ``libfp8bs.so`` (C ABI:
 ``include/fp8bs.h``); ``binding`` marshals torch tensors to it, ``linear``
-chains the calls into one linear layer's forward and backward step, and
+chains the calls into one linear layer's forward and backward step (also as
+a torch autograd op and module), and
 ``inputs`` draws the seeded synthetic workloads.  Importing the package does
 not load the library; the first call does, and fails if it is missing.
 """
@@ -22,12 +23,14 @@ _BINDING_NAMES = (
     "fp8bs_gemm_wgrad_accumulate_f32",
 )
 
-__all__ = list(_BINDING_NAMES) + ["Fp8LinearStep"]
+_LINEAR_NAMES = ("Fp8LinearStep", "Fp8LinearFunction", "Fp8Linear")
+
+__all__ = list(_BINDING_NAMES) + list(_LINEAR_NAMES)
 
 
 def __getattr__(name):
     if name in _BINDING_NAMES:
         return getattr(importlib.import_module(".binding", __name__), name)
-    if name == "Fp8LinearStep":
-        return importlib.import_module(".linear", __name__).Fp8LinearStep
+    if name in _LINEAR_NAMES:
+        return getattr(importlib.import_module(".linear", __name__), name)
     raise AttributeError(name)

@@ -137,3 +137,67 @@ def interleave_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor) -> torch.Tensor
     if tuple(w_up.shape) != (I, K) or I % 128:
         raise ValueError("gate and up weights must both be [I][K] with I a multiple of 128")
     return torch.stack([w_gate.reshape(I // 128, 128, K), w_up.reshape(I // 128, 128, K)], 1).reshape(2 * I, K)
+
+
+class Fp8LinearFunction(torch.autograd.Function):
+    """y = x W^T through the FP8 block-scaled path, as a torch autograd op.
+
+    forward : X -> 1x128 (and, if W needs a gradient, 128x1 transposed) in one
+              read; W -> 128x128 blocks (and W^T if X needs a gradient);
+              Y = fp8bs_gemm_fprop.
+    backward: dY -> 1x128 (for dX) and/or 128x1 transposed (for dW) in one
+              read; dX = fp8bs_gemm_dgrad, dW = fp8bs_gemm_wgrad.
+
+    x: BF16 CUDA tensor [..., K]; w: BF16 [N][K]; K and N multiples of 128,
+    any number of tokens.  Only the quantized operands the backward needs are
+    kept (Xq^T and its scales, Wq^T and the block scales): 1 byte per element
+    instead of the BF16 originals.  Every arithmetic step runs in the
+    library's kernels; this class only orders the calls."""
+
+    @staticmethod
+    def forward(ctx, x, w):
+        K = x.shape[-1]
+        N = w.shape[0]
+        if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or not x.is_cuda:
+            raise TypeError("Fp8LinearFunction takes BF16 CUDA tensors")
+        if tuple(w.shape) != (N, K) or K % 128 or N % 128:
+            raise ValueError("w must be [N][K] with N and K multiples of 128, x [..., K]")
+        x2 = x.reshape(-1, K).contiguous()
+        need_dw, need_dx = ctx.needs_input_grad[1], ctx.needs_input_grad[0]
+        xq, sx, xTq, sxT = B.fp8bs_quantize_act(x2, B.ROWWISE | (B.COLWISE_T if need_dw else 0))
+        wq, wqT, sw = B.fp8bs_quantize_weight(w.contiguous(), want_t=need_dx)
+        y = B.fp8bs_gemm_fprop(xq, sx, wq, sw)
+        ctx.save_for_backward(xTq, sxT, wqT, sw)
+        ctx.x_shape, ctx.M, ctx.N, ctx.K = x.shape, x2.shape[0], N, K
+        return y.reshape(*x.shape[:-1], N)
+
+    @staticmethod
+    def backward(ctx, dy):
+        xTq, sxT, wqT, sw = ctx.saved_tensors
+        need_dx, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        dy2 = dy.reshape(-1, ctx.N)
+        if dy2.dtype != torch.bfloat16:
+            dy2 = dy2.to(torch.bfloat16)
+        dy2 = dy2.contiguous()
+        flags = (B.ROWWISE if need_dx else 0) | (B.COLWISE_T if need_dw else 0)
+        dyq, sdy, dyTq, sdyT = B.fp8bs_quantize_act(dy2, flags)
+        dx = B.fp8bs_gemm_dgrad(dyq, sdy, wqT, sw).reshape(ctx.x_shape) if need_dx else None
+        dw = B.fp8bs_gemm_wgrad(dyTq, sdyT, xTq, sxT) if need_dw else None
+        return dx, dw
+
+
+class Fp8Linear(torch.nn.Module):
+    """A bias-free linear layer whose forward and backward GEMMs run on the
+    FP8 block-scaled path (the weight is kept in BF16 and quantized in every
+    forward)."""
+
+    def __init__(self, in_features: int, out_features: int, device="cuda", std: float = 0.02):
+        super().__init__()
+        if in_features % 128 or out_features % 128:
+            raise ValueError("in_features and out_features must be multiples of 128")
+        self.in_features, self.out_features = in_features, out_features
+        self.weight = torch.nn.Parameter(
+            torch.randn(out_features, in_features, device=device, dtype=torch.float32).mul_(std).to(torch.bfloat16))
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return Fp8LinearFunction.apply(x, self.weight)

@@ -71,3 +71,15 @@ def test_interleave_gate_up_row_order():
         assert torch.equal(w[256 * j + 128:256 * j + 256], wu[128 * j:128 * j + 128])
     with pytest.raises(ValueError):
         interleave_gate_up(wg[:100], wu[:100])
+
+
+def test_autograd_wrapper_checks_its_arguments():
+    from fp8_block_scaled_16_b300.linear import Fp8Linear, Fp8LinearFunction
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    w = torch.zeros(128, 256, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        Fp8LinearFunction.apply(x, w)              # CPU tensors: the path is CUDA only
+    with pytest.raises(TypeError):
+        Fp8LinearFunction.apply(x.float(), w)      # not BF16
+    with pytest.raises(ValueError):
+        Fp8Linear(200, 128, device="cpu")          # not a multiple of 128
