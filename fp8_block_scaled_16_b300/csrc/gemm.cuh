@@ -124,7 +124,7 @@ struct Tile {
     static constexpr int OUT_BOX_BYTES = 32 * 64 * 2;
     static constexpr int OFF_OUT = (OFF_SCALE + SSLOTS * SLOT_FLOATS * 4 + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_OUT + NUM_EPI_WARPS * 2 * OUT_BOX_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + NBUF + 2 * SSLOTS + 12;
+    static constexpr int NUM_BARS = 2 * STAGES + NBUF + 2 * SSLOTS + 14;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     // SwiGLU epilogue: per quadrant and column half, the 32 rows' partial amax
     // of H as BF16 bits (H is BF16, so its amax is too).
@@ -150,6 +150,11 @@ struct Tile {
     static __device__ __forceinline__ uint32_t xhalf(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + q; }
     static __device__ __forceinline__ uint32_t xamax(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + 4 + q; }
     static __device__ __forceinline__ uint32_t xq8(int q) { return 2 * STAGES + NBUF + 2 * SSLOTS + 8 + q; }
+    // Plain BF16 epilogue with its TMA stores issued by warp 3: ofull -- every
+    // promotion warp has staged its slice of the tile; ofree -- those stores
+    // have read the staging buffer.
+    static __device__ __forceinline__ uint32_t ofull() { return 2 * STAGES + NBUF + 2 * SSLOTS + 12; }
+    static __device__ __forceinline__ uint32_t ofree() { return 2 * STAGES + NBUF + 2 * SSLOTS + 13; }
 };
 
 struct Params {
@@ -210,27 +215,35 @@ struct Unit {
 __device__ __forceinline__ int num_units_of(const Params& p, int num_tiles) {
     return p.tail_first + p.splits * (num_tiles - p.tail_first);
 }
+// Every role decodes its next unit at each tile boundary, on the path the
+// tensor pipe waits on, so whole tiles take no division at all, and split
+// parts only 32-bit ones (s < 8 and kblocks < 2^24: s * kblocks < 2^27).
 __device__ __forceinline__ Unit unit_of(int u, const Params& p, int num_tiles) {
     Unit w;
     w.s = 0;
     w.split = false;
     w.kb0 = 0;
     w.kb1 = p.kblocks;
-    if (u < p.tail_first) {
+    if (p.splits == 1 || u < p.tail_first) {
         w.t = u;
         return w;
     }
     const int v = u - p.tail_first, nt = num_tiles - p.tail_first;
     w.s = v / nt;
     w.t = p.tail_first + v - w.s * nt;
-    w.split = p.splits > 1;
-    w.kb0 = static_cast<int>(static_cast<int64_t>(w.s) * p.kblocks / p.splits);
-    w.kb1 = static_cast<int>(static_cast<int64_t>(w.s + 1) * p.kblocks / p.splits);
+    w.split = true;
+    w.kb0 = (w.s * p.kblocks) / p.splits;
+    w.kb1 = ((w.s + 1) * p.kblocks) / p.splits;
     return w;
 }
 
 // Output tile t's row and column block under the strip order of Params::strip.
 __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
+    if (p.strip == p.n_tiles) {  // row-major: one division
+        mb = t / p.n_tiles;
+        nb = t - mb * p.n_tiles;
+        return;
+    }
     const int per_strip = p.m_tiles * p.strip;
     const int strip = t / per_strip, local = t - strip * per_strip;
     const int width = min(p.strip, p.n_tiles - strip * p.strip);
@@ -378,6 +391,58 @@ __device__ __forceinline__ void promote_rank1(float (&acc)[N], int base_lo, int 
     }
 }
 
+// The plain BF16 epilogue of unit w is staged by the promotion warps and
+// stored by warp 3 (the output store issuer) unless the unit is a part of a
+// split tile (whose last part, found at run time, stores it) or the output
+// is FP32.  Both sides take the same decision from the same unit.
+__device__ __forceinline__ bool delegated_store(const Params& p, const Unit& w) {
+    return !w.split && p.out_f32_add == 0 && p.out_bf16 != 0;
+}
+
+// A promotion warp's 32 x 128 slice of the tile in BF16 into its two
+// 32-row x 64-column staging boxes (4 KB each, 128-byte swizzle: the
+// 16-byte chunk c of row r at chunk c ^ (r % 8), so the lanes' writes
+// spread over all banks), from the .32x32b (SB_SCALAR) or .16x256b
+// (SB_VECTOR) accumulator layout.
+template <int SBMODE, int N>
+__device__ __forceinline__ void stage_bf16_tile(const float (&acc)[N], uint32_t stage_out, int lane) {
+    constexpr uint32_t kBox = 32 * 64 * 2;
+    if constexpr (SBMODE == SB_SCALAR) {
+#pragma unroll
+        for (int b = 0; b < 2; b++) {
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                const int j = b * 64 + c * 8;
+                const uint32_t w0 = f32x2_to_bf16x2(acc[j + 0], acc[j + 1]);
+                const uint32_t w1 = f32x2_to_bf16x2(acc[j + 2], acc[j + 3]);
+                const uint32_t w2 = f32x2_to_bf16x2(acc[j + 4], acc[j + 5]);
+                const uint32_t w3 = f32x2_to_bf16x2(acc[j + 6], acc[j + 7]);
+                const uint32_t a = stage_out + static_cast<uint32_t>(b * kBox + lane * 128 + ((c ^ (lane & 7)) << 4));
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                             : "memory");
+            }
+        }
+    } else {
+        // .16x256b layout: acc[32L + 4g + 2hi], {+1} is row 16(L/2) + 8hi + t/4,
+        // columns 64(L%2) + 8g + 2(t%4) + {0,1}: one BF16 pair per store, the
+        // eight rows of a store in eight different 16-byte chunks.
+        const int u = lane >> 2, c = lane & 3;
+#pragma unroll
+        for (int L = 0; L < 4; L++) {
+#pragma unroll
+            for (int g = 0; g < 8; g++) {
+#pragma unroll
+                for (int hi = 0; hi < 2; hi++) {
+                    const int j = 32 * L + 4 * g + 2 * hi;
+                    const int rr = 16 * (L >> 1) + 8 * hi + u;
+                    const uint32_t a = stage_out + static_cast<uint32_t>((L & 1) * kBox + rr * 128 + ((g ^ u) << 4) + 4 * c);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(f32x2_to_bf16x2(acc[j], acc[j + 1])) : "memory");
+                }
+            }
+        }
+    }
+}
+
 // SwiGLU epilogue helpers (one 64-column half of a warp's 128 accumulator
 // columns, offsets fixed at compile time so that acc stays in registers).
 // A staging box row is 128 bytes: 16-byte chunk c of row r at c ^ (r % 8).
@@ -470,6 +535,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             mbar_init(bar(T::xamax(q)), 2);
             mbar_init(bar(T::xq8(q)), 1);
         }
+        mbar_init(bar(T::ofull()), NUM_EPI_WARPS);
+        mbar_init(bar(T::ofree()), 1);
         for (int i = 0; i < SSLOTS; i++) {
             mbar_init(bar(T::sfull(i)), 32);   // one cp.async arrival per lane of the scale warp
             mbar_init(bar(T::sempty(i)), NUM_EPI_WARPS);
@@ -644,6 +711,39 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             }
         }
         cp_async_wait_all();
+      } else if constexpr (EPI == EPI_PLAIN) {
+        // ------------------------------------------------ output store issuer
+        // For the units whose plain BF16 epilogue it takes over (delegated_store),
+        // waits until every promotion warp has staged its slice, issues the
+        // tile's TMA stores, and frees the staging buffer once they have read
+        // it, so that the promotion warps go on to the next tile at once.
+        uint32_t oph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+            FP8BS_UNIT(u);
+            if (!delegated_store(p, w)) continue;
+            int mb, nb;
+            tile_coords(w.t, p, mb, nb);
+            if (!uniform_wait(bar(T::ofull()), oph, wc)) { ok = false; break; }
+            if (lane == 0) {
+#pragma unroll 1
+                for (int e = 0; e < NUM_EPI_WARPS; e++) {
+                    const int q = e & 3, h = e >> 2;
+                    const int32_t x0 = nb * BN + h * COLS, y0 = mb * BM + q * 32;
+                    if ((x0 >> 7) >= p.nb_valid || static_cast<int64_t>(y0) >= p.rows) continue;
+                    const uint32_t so = sbase + T::OFF_OUT + static_cast<uint32_t>(e * 2 * T::OUT_BOX_BYTES);
+                    tma_store_2d(&grp.tmC[g], so, x0, y0);
+                    tma_store_2d(&grp.tmC[g], so + T::OUT_BOX_BYTES, x0 + 64, y0);
+                }
+                bulk_commit_group();
+                bulk_wait_read_all();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(T::ofree()));
+            oph ^= 1u;
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
@@ -655,6 +755,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         const float* ring = reinterpret_cast<const float*>(smem + T::OFF_SCALE);
         int tb = 0, slot = 0, stage = 0;
         uint32_t sph = 0, xph = 0, q8ph = 0, ph = 0;
+        uint32_t delegated = 0;  // units whose stores warp 3 issued so far
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             FP8BS_UNIT(u);
@@ -866,6 +967,23 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
             // Output boxes that lie wholly past the last row (a token tail) are
             // not stored; TMA clips the rows of a partial box.
             const bool rvalid = static_cast<int64_t>(mb) * BM + quad * 32 < p.rows;
+            // The staging buffer is free once warp 3's stores of the last
+            // delegated unit have read it (the wait is satisfied at once when
+            // they already have).
+            if (delegated > 0 && !uniform_wait(bar(T::ofree()), (delegated - 1) & 1u, wc)) { ok = false; break; }
+            if constexpr (EPI == EPI_PLAIN) {
+                if (delegated_store(p, w)) {
+                    const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
+                    if (jvalid && rvalid) {
+                        stage_bf16_tile<SBMODE>(acc, stage_out, lane);
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T::ofull()));
+                    delegated++;
+                    continue;
+                }
+            }
             if (jvalid && rvalid && p.out_f32_add) {
                 // FP32 accumulate: four 32-row x 32-column boxes per warp, staged two
                 // at a time (same 8 KB buffer, 128-byte swizzle: 16-byte chunk c of
@@ -933,44 +1051,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
                 const uint32_t stage_out = sbase + T::OFF_OUT + static_cast<uint32_t>(ew * 2 * T::OUT_BOX_BYTES);
                 if (lane == 0) bulk_wait_read_all();  // the previous tile's stores have read the buffer
                 __syncwarp();
-                if constexpr (SBMODE == SB_SCALAR) {
-#pragma unroll
-                    for (int b = 0; b < 2; b++) {
-#pragma unroll
-                        for (int c = 0; c < 8; c++) {
-                            const int j = b * 64 + c * 8;
-                            const uint32_t w0 = f32x2_to_bf16x2(acc[j + 0], acc[j + 1]);
-                            const uint32_t w1 = f32x2_to_bf16x2(acc[j + 2], acc[j + 3]);
-                            const uint32_t w2 = f32x2_to_bf16x2(acc[j + 4], acc[j + 5]);
-                            const uint32_t w3 = f32x2_to_bf16x2(acc[j + 6], acc[j + 7]);
-                            const uint32_t a = stage_out + static_cast<uint32_t>(b * T::OUT_BOX_BYTES + lane * 128 +
-                                                                                 ((c ^ (lane & 7)) << 4));
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1),
-                                         "r"(w2), "r"(w3)
-                                         : "memory");
-                        }
-                    }
-                } else {
-                    // .16x256b layout: acc[32L + 4g + 2hi], {+1} is row 16(L/2) + 8hi + t/4,
-                    // columns 64(L%2) + 8g + 2(t%4) + {0,1}: one BF16 pair per store, the
-                    // eight rows of a store in eight different 16-byte chunks.
-                    const int u = lane >> 2, c = lane & 3;
-#pragma unroll
-                    for (int L = 0; L < 4; L++) {
-#pragma unroll
-                        for (int g = 0; g < 8; g++) {
-#pragma unroll
-                            for (int hi = 0; hi < 2; hi++) {
-                                const int j = 32 * L + 4 * g + 2 * hi;
-                                const int rr = 16 * (L >> 1) + 8 * hi + u;
-                                const uint32_t a = stage_out + static_cast<uint32_t>((L & 1) * T::OUT_BOX_BYTES +
-                                                                                     rr * 128 + ((g ^ u) << 4) + 4 * c);
-                                asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(f32x2_to_bf16x2(acc[j], acc[j + 1]))
-                                             : "memory");
-                            }
-                        }
-                    }
-                }
+                stage_bf16_tile<SBMODE>(acc, stage_out, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
