@@ -24,8 +24,9 @@
 //       weight scales of 4 consecutive K blocks; weight gradient, per slot
 //       one K block's 128 row scales and 256 column scales (regrouped for
 //       the epilogue's layout);
-//   warp 3: idle (it completes the first warpgroup, whose registers are
-//       handed to the epilogue warpgroups with setmaxnreg);
+//   warp 3: output store issuer -- for whole tiles with a plain BF16
+//       output, the tile's TMA stores once every promotion warp has staged
+//       its slice, so that the promotion warps start the next tile at once;
 //   warps 4..11: promotion + epilogue -- each warp owns a 32-lane TMEM
 //       quadrant (rows) and one 128-column half; per K block it loads its
 //       partial with tcgen05.ld, 64 columns at a time (.32x32b: a row per
