@@ -75,17 +75,22 @@ constexpr int BM = 128, BK = 128;
 constexpr int SSLOTS = 8;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 128 + NUM_EPI_WARPS * 32;
-// Register split after launch (launch: 168 per thread = 384 x 168 total).
-// Per SM sub-partition: one first-warpgroup warp and two epilogue warps,
-// 48 + 2 x 224 = 496 <= 512 registers per lane slot; CTA-wide
-// 128 x 48 + 256 x 224 = 63488 <= 64512.
-constexpr int REGS_CTRL = 48;
-constexpr int REGS_EPI = 224;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(THREADS == 384, "warp roles");
-static_assert(128 * REGS_CTRL + NUM_EPI_WARPS * 32 * REGS_EPI <= THREADS * 168, "register split");
 
 enum : int { SB_SCALAR = 0, SB_VECTOR = 1 };
+
+// Register split after launch (168 per thread at launch, 384 x 168 = 64512 in
+// all): `ctrl` for the four first-warpgroup warps, `epi` for the eight
+// promotion warps.  The weight gradient's promotion holds 128 accumulators,
+// 64 loaded values and its scales at once; at 224 registers it spills, so its
+// kernels give it 232 and the first warpgroup 40.
+template <int SBMODE>
+struct RegSplit {
+    static constexpr int ctrl = SBMODE == SB_VECTOR ? 40 : 48;
+    static constexpr int epi = SBMODE == SB_VECTOR ? 232 : 224;
+    static_assert(128 * ctrl + NUM_EPI_WARPS * 32 * epi <= THREADS * 168, "register split");
+};
 // Epilogue variants of the forward product, each its own kernel so that the
 // plain kernel carries none of the others' code: the tile as BF16 (or FP32
 // reduce-adds); plus its 1x128 FP8 quantization; the SwiGLU block instead.
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     const Unit w = unit_of((u) - grp.first_unit[g], p, num_tiles)
 
     if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegSplit<SBMODE>::ctrl));
       // The producer and MMA warps run their loops with all 32 lanes
       // converged (waits are warp-wide); only lane 0 issues the TMA and
       // tcgen05 instructions.  A lone lane looping while its warp-mates
@@ -747,7 +752,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         __syncwarp();
       }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegSplit<SBMODE>::epi));
         // ------------------------------------------------ promotion + epilogue
         const int ew = warp - 4;
         const int quad = warp & 3;   // TMEM lanes this warp may access
