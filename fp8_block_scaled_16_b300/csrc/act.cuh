@@ -55,11 +55,19 @@ __device__ __forceinline__ float2 exp_cw2(float2 x) {
     return e;
 }
 
-// FP32 h = SiLU(g) * u = g / (1 + e^-g) * u for two pairs of BF16-valued g
-// and u (before the final rounding): one IEEE rounding per operation.
-__device__ __forceinline__ float2 silu_mul2_f32(float2 g, float2 u) {
-    const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), exp_cw2(make_float2(-g.x, -g.y)));
+// The two steps of h = SiLU(g) * u = g / (1 + e^-g) * u for two pairs of
+// BF16-valued g and u (before the final rounding), one IEEE rounding per
+// operation: the denominator 1 + e^-g, then the quotient times u.
+__device__ __forceinline__ float2 silu_denom2(float2 g) {
+    return __fadd2_rn(make_float2(1.0f, 1.0f), exp_cw2(make_float2(-g.x, -g.y)));
+}
+
+__device__ __forceinline__ float2 silu_mul2_from_denom(float2 g, float2 d, float2 u) {
     return __fmul2_rn(make_float2(__fdiv_rn(g.x, d.x), __fdiv_rn(g.y, d.y)), u);
+}
+
+__device__ __forceinline__ float2 silu_mul2_f32(float2 g, float2 u) {
+    return silu_mul2_from_denom(g, silu_denom2(g), u);
 }
 
 // Test kernel: h[i] = bf16(SiLU(g[i]) * u[i]) on BF16 bit patterns, two

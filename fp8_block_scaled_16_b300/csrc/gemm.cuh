@@ -467,7 +467,10 @@ __device__ __forceinline__ void stage_bf16_64(const float (&acc)[N], uint32_t bo
 
 // H = bf16(SiLU(G) * U) for acc[J0 .. J0+63] (this warp's gate values if
 // GATE, else its up values) with the other operand's BF16 half from `peer`;
-// the BF16 H values replace acc and their amax is returned.
+// the BF16 H values replace acc and their amax is returned.  Per 8-value
+// chunk the four exponentials come first and the eight divisions after, so
+// that the exponentials' dependent chains overlap; each value still takes
+// the same operations in the same order.
 template <int J0, bool GATE, int N>
 __device__ __forceinline__ float swiglu_64(float (&acc)[N], uint32_t peer, int lane) {
     float amax = 0.0f;
@@ -480,13 +483,19 @@ __device__ __forceinline__ float swiglu_64(float (&acc)[N], uint32_t peer, int l
                      : "=r"(pw[0]), "=r"(pw[1]), "=r"(pw[2]), "=r"(pw[3])
                      : "r"(a)
                      : "memory");
+        float2 gv[4], uv[4], dv[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             const uint32_t ow = f32x2_to_bf16x2(acc[j + 2 * e], acc[j + 2 * e + 1]);
             const uint32_t gw = GATE ? ow : pw[e];
             const uint32_t uw = GATE ? pw[e] : ow;
-            const float2 h = silu_mul2_f32(make_float2(bf16lo_to_f32(gw), bf16hi_to_f32(gw)),
-                                           make_float2(bf16lo_to_f32(uw), bf16hi_to_f32(uw)));
+            gv[e] = make_float2(bf16lo_to_f32(gw), bf16hi_to_f32(gw));
+            uv[e] = make_float2(bf16lo_to_f32(uw), bf16hi_to_f32(uw));
+            dv[e] = silu_denom2(gv[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float2 h = silu_mul2_from_denom(gv[e], dv[e], uv[e]);
             const uint32_t hw = f32x2_to_bf16x2(h.x, h.y);
             acc[j + 2 * e] = bf16lo_to_f32(hw);
             acc[j + 2 * e + 1] = bf16hi_to_f32(hw);
