@@ -71,6 +71,36 @@ MUTANTS = [
     ("e^x polynomial without its r^2/2 term",
      "p = fmaf(p, r, 0.5f);",
      "p = fmaf(p, r, 0.0f);"),
+    ("row-wise amax of signed values",
+     "float a = fabsf(orc_bf16_to_f32(t[i]));",
+     "float a = orc_bf16_to_f32(t[i]);"),
+    ("weight amax over the block's first column only",
+     "float a = fabsf(orc_bf16_to_f32(w[(bn * 128 + i) * k + bk * 128 + j]));",
+     "float a = fabsf(orc_bf16_to_f32(w[(bn * 128 + i) * k + bk * 128]));"),
+    ("row-wise scales stored row-major",
+     "            s[b * mp + r] = sc;",
+     "            s[r * nb + b] = sc;"),
+    ("128x1 scales stored column-major",
+     "sT[b * cols + c] = sc;",
+     "sT[c * nb + b] = sc;"),
+    ("weight scales stored transposed",
+     "s[bn * nbk + bk] = sc;",
+     "s[bk * nbn + bn] = sc;"),
+    ("E4M3 drops the sign of a value that rounds to zero",
+     "        return (uint8_t)(sign | m);",
+     "        return (uint8_t)(m ? (sign | m) : 0u);"),
+    ("wgrad applies the row scale twice",
+     "sdyt + n, N,\n                                  sxt + k, K, &sabs);",
+     "sdyt + n, N,\n                                  sdyt + n, N, &sabs);"),
+    ("dgrad weight scale of the transposed block",
+     "sw + k / 128, kb, &sabs);",
+     "sw + (k / 128) * kb, 1, &sabs);"),
+    ("e^x without the low part of ln 2",
+     "    r = fmaf(-n, LN2_LO_F, r);\n",
+     ""),
+    ("SiLU rounds g / (1 + e^-g) to BF16 before the product",
+     "    float sg = g / d;\n",
+     "    float sg = orc_bf16_to_f32(orc_f32_to_bf16(g / d));\n"),
 ]
 
 
